@@ -1,0 +1,538 @@
+"""Throughput of the fused GEMM / conv + bias + activation path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mmact|reference]
+                    [--workload NAME] [--no-sweep] [--no-e2e] [--no-cpu-baseline]
+
+One step = one fused launch (C = act(A x B + bias)) over the workload's
+synthetic inputs, which stay resident in HBM.  Rank 0 prints one JSON line.
+Under torchrun every rank runs its own replica of the workload on its own GPU
+(the problems are independent: no collective on the data path), so scaling
+is weak and `value` is the whole job's throughput.
+
+`--impl reference` times the CPU oracle instead (the plain fp64 routine the
+tests check the kernels against), on a bounded sample of the same workload,
+on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from conv_activation_epilogue_gb300 import synth  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "fused GEMM/conv+act TFLOP/s and % of GB300 dense bf16 tensor peak (1 GPU)"
+KERNEL_SOURCES = ["common.cuh", "ptx.cuh", "gemm.cu", "conv.cu", "elementwise.cu", "api.cu"]
+
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "conv_activation_epilogue_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(f"{kernel}/{workload}")
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- GPU helpers --
+def torch_dtype(torch, name):
+    return {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[name]
+
+
+def codes_to(torch, codes, dt, device, pin=False):
+    t = torch.from_numpy(np.ascontiguousarray(codes).view(np.int16)).view(torch_dtype(torch, dt))
+    if device == "cpu":
+        return t.pin_memory() if pin else t
+    return t.to(device)
+
+
+def workload_flops(mmact, wl):
+    if wl.kind == "gemm":
+        return 2.0 * wl.M * wl.N * wl.K
+    Ho, Wo = mmact.mmact_conv2d_out_shape(wl.H, wl.W, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation)
+    return 2.0 * wl.N * Ho * Wo * wl.Co * wl.C * wl.kh * wl.kw
+
+
+def workload_bytes(mmact, wl):
+    """Algorithmic HBM bytes: read every input once, write the output once."""
+    ob = 4 if (wl.c_dtype if wl.kind == "gemm" else wl.out_dtype) == "f32" else 2
+    if wl.kind == "gemm":
+        return 2.0 * (wl.M * wl.K + wl.K * wl.N) + 4.0 * wl.N + ob * wl.M * wl.N
+    Ho, Wo = mmact.mmact_conv2d_out_shape(wl.H, wl.W, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation)
+    return (2.0 * (wl.N * wl.C * wl.H * wl.W + wl.Co * wl.C * wl.kh * wl.kw) + 4.0 * wl.Co +
+            ob * wl.N * wl.Co * Ho * Wo)
+
+
+class Problem:
+    """Device-resident inputs/outputs of one workload and a launcher per variant."""
+
+    def __init__(self, torch, mmact, wl, device, inputs=None):
+        self.torch, self.mmact, self.wl, self.device = torch, mmact, wl, device
+        inp = inputs if inputs is not None else wl.inputs()
+        self.host = inp
+        if wl.kind == "gemm":
+            self.A = codes_to(torch, inp["A"], wl.ab_dtype, device)
+            self.B = codes_to(torch, inp["B"], wl.ab_dtype, device)
+            self.bias = torch.from_numpy(inp["bias"]).to(device)
+            self.out = torch.empty((wl.M, wl.N), dtype=torch_dtype(torch, wl.c_dtype), device=device)
+        else:
+            self.x = codes_to(torch, inp["x"], wl.dtype, device)
+            self.w = codes_to(torch, inp["w"], wl.dtype, device)
+            self.bias = torch.from_numpy(inp["bias"]).to(device)
+            Ho, Wo = mmact.mmact_conv2d_out_shape(wl.H, wl.W, wl.kh, wl.kw, wl.stride, wl.pads,
+                                                  wl.dilation)
+            self.out = torch.empty((wl.N, wl.Co, Ho, Wo), dtype=torch_dtype(torch, wl.out_dtype),
+                                   device=device)
+        self.ws = None
+
+    def workspace(self):
+        if self.ws is None:
+            self.ws = self.torch.empty((self.out.numel(),), dtype=self.torch.float32, device=self.device)
+        return self.ws
+
+    def run(self, variant="fused", stream=None):
+        wl, m = self.wl, self.mmact
+        if wl.kind == "gemm":
+            if variant == "fused":
+                m.mmact_gemm(self.A, self.B, self.bias, self.out, wl.act, wl.alpha, stream)
+            else:
+                m.mmact_gemm_split(self.A, self.B, self.bias, self.out, self.workspace(), wl.act,
+                                   wl.alpha, stream)
+        else:
+            if variant == "fused":
+                m.mmact_conv2d(self.x, self.w, self.bias, self.out, wl.stride, wl.pads, wl.dilation,
+                               wl.act, wl.alpha, stream)
+            else:
+                m.mmact_conv2d_split(self.x, self.w, self.bias, self.out, self.workspace(), wl.stride,
+                                     wl.pads, wl.dilation, wl.act, wl.alpha, stream)
+
+    def input_bytes(self):
+        if self.wl.kind == "gemm":
+            return sum(t.numel() * t.element_size() for t in (self.A, self.B, self.bias))
+        return sum(t.numel() * t.element_size() for t in (self.x, self.w, self.bias))
+
+
+def time_launches(torch, fn, steps, warmup, stream):
+    """Average ms per call of fn() over `steps` calls, CUDA events on `stream`."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def time_graph(torch, fn, reps, stream):
+    """Average ms per call of fn(), replaying a CUDA graph of `reps` back-to-back calls
+    (no host launch overhead between them); CUDA events on `stream`."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.graph(g, stream=cap):
+        for _ in range(reps):
+            fn()
+    stream.wait_stream(cap)
+    g.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(3):
+        g.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / (3 * reps)
+
+
+def parity_spot_check(oracle_mod, prob, npts=256, seed=99):
+    """Compare a few sampled outputs of the timed launch with the oracle (max err / bound)."""
+    wl = prob.wl
+    out = prob.out.float().cpu().numpy().astype(np.float64).ravel()
+    rng = np.random.default_rng(seed)
+    pts = rng.integers(0, out.size, size=npts)
+    orc = oracle_mod.get()
+    h = prob.host
+    if wl.kind == "gemm":
+        ref = orc.gemm(h["A"], h["B"], wl.ab_dtype, h["bias"], wl.act, wl.alpha, points=pts)
+        od = wl.c_dtype
+    else:
+        ref = orc.conv2d(h["x"], h["w"], wl.dtype, h["bias"], wl.stride, wl.pads, wl.dilation,
+                         wl.act, wl.alpha, points=pts)
+        od = wl.out_dtype
+    a = np.abs(ref)
+    ulp = 0.0 if od == "f32" else np.exp2(np.floor(np.log2(np.where(a > 0, a, 1.0))) -
+                                           (7 if od == "bf16" else 10))
+    ratio = np.abs(out[pts] - ref) / (2e-3 + 2e-3 * a + ulp)
+    return float(ratio.max())
+
+
+# --------------------------------------------------------- reference (CPU) --
+def oracle_sample_run(oracle_mod, wl, inputs, n_points, threads, seed):
+    """Evaluate n_points output elements of the workload with the oracle; returns seconds."""
+    rng = np.random.default_rng(seed)
+    orc = oracle_mod.get()
+    if wl.kind == "gemm":
+        pts = rng.integers(0, wl.M * wl.N, size=n_points)
+        t0 = time.perf_counter()
+        orc.gemm(inputs["A"], inputs["B"], wl.ab_dtype, inputs["bias"], wl.act, wl.alpha,
+                 points=pts, threads=threads)
+    else:
+        x = inputs["x"]
+        Ho = orc.conv_out_dim(wl.H, wl.kh, wl.stride[0], wl.pads[0], wl.pads[1], wl.dilation[0])
+        Wo = orc.conv_out_dim(wl.W, wl.kw, wl.stride[1], wl.pads[2], wl.pads[3], wl.dilation[1])
+        pts = rng.integers(0, wl.N * wl.Co * Ho * Wo, size=n_points)
+        t0 = time.perf_counter()
+        orc.conv2d(x, inputs["w"], wl.dtype, inputs["bias"], wl.stride, wl.pads, wl.dilation,
+                   wl.act, wl.alpha, points=pts, threads=threads)
+    return time.perf_counter() - t0
+
+
+def flops_per_output(wl):
+    if wl.kind == "gemm":
+        return 2.0 * wl.K
+    return 2.0 * wl.C * wl.kh * wl.kw
+
+
+def calibrate_points(oracle_mod, wl, inputs, threads, target_s):
+    n = 64
+    while True:
+        dt = oracle_sample_run(oracle_mod, wl, inputs, n, threads, seed=1)
+        if dt > 0.25 or n >= 1 << 22:
+            break
+        n *= 4
+    return max(16, int(n * target_s / max(dt, 1e-6)))
+
+
+def cpu_baseline(wl, inputs, target_s=15.0):
+    import oracle as oracle_mod
+    threads = os.cpu_count() or 1
+    n = calibrate_points(oracle_mod, wl, inputs, threads, target_s)
+    dt = oracle_sample_run(oracle_mod, wl, inputs, n, threads, seed=2)
+    value = n * flops_per_output(wl) / dt / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} output elements of {wl.name} drawn uniformly at random "
+                      f"({flops_per_output(wl):.0f} flop each), fp64, {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank = env_int("RANK", 0)
+    if rank != 0:
+        return 0
+    import oracle as oracle_mod
+    wl = synth.WORKLOADS[args.workload]
+    inputs = wl.inputs()
+    threads = os.cpu_count() or 1
+    n = calibrate_points(oracle_mod, wl, inputs, threads, target_s=2.0)
+    for i in range(args.warmup):
+        oracle_sample_run(oracle_mod, wl, inputs, n, threads, seed=100 + i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_sample_run(oracle_mod, wl, inputs, n, threads, seed=1000 + i)
+    total = time.perf_counter() - t0
+    ms = total / args.steps * 1e3
+    value = n * flops_per_output(wl) * args.steps / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "step": f"{n} sampled output elements (oracle)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} output elements of {wl.name} per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------------- main --
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mmact", choices=["mmact", "reference"])
+    ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    from conv_activation_epilogue_gb300 import build, mmact
+
+    rank, world, local = env_int("RANK", 0), env_int("WORLD_SIZE", 1), env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    build.build()
+    mmact.load()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    wl = synth.WORKLOADS[args.workload]
+    prob = Problem(torch, mmact, wl, device)
+    flops = workload_flops(mmact, wl)
+    stream = torch.cuda.current_stream()
+
+    # --- timed region: K fused launches, inputs resident, > L2 so no flush needed
+    for _ in range(args.warmup):
+        prob.run("fused")
+    torch.cuda.synchronize()
+    st = mmact.mmact_get_last_error()
+    if st != mmact.MMACT_OK:
+        raise RuntimeError(f"kernel status {mmact.mmact_status_string(st)}")
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        prob.run("fused")
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clock_rec = clocks.stop()
+    ms = start.elapsed_time(end) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    st = mmact.mmact_get_last_error()
+    if st != mmact.MMACT_OK:
+        raise RuntimeError(f"kernel status {mmact.mmact_status_string(st)}")
+
+    import oracle as oracle_mod
+    parity = parity_spot_check(oracle_mod, prob) if rank == 0 else None
+
+    value = world * flops / (ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    achieved = flops / (ms * 1e-3) / 1e12        # one launch per step
+    kname = "gemm_act_kernel" if wl.kind == "gemm" else "conv_act_kernel"
+    in_bytes = prob.input_bytes()
+
+    # --- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(torch, mmact, wl, prob, device, stream, args, flops, world, barrier, dist)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.ab_dtype if wl.kind == "gemm" else wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "variant": "fused single kernel",
+                   "l2": "inputs larger than L2, no flush" if in_bytes > L2_BYTES
+                   else "inputs smaller than L2, no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "pct_of_bf16_peak": round(100.0 * achieved / peaks["bf16_tflops"], 2)},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "traffic": traffic_per_launch(kname, wl.name),
+                     "kernel": kname, "peak_source": f"{peak_src} burst bf16"},
+        "parity_max_err_over_bound": parity,
+        "clocks": clock_rec,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_sweep:
+        line["sweep"] = sweep(torch, mmact, device, stream, peaks)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, prob.host)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def end_to_end(torch, mmact, wl, prob, device, stream, args, flops, world, barrier, dist):
+    """Same metric through the public API with pinned host buffers: H2D, launch, D2H per step."""
+    h = prob.host
+    if wl.kind == "gemm":
+        hA = codes_to(torch, h["A"], wl.ab_dtype, "cpu", pin=True)
+        hB = codes_to(torch, h["B"], wl.ab_dtype, "cpu", pin=True)
+        hb = torch.from_numpy(h["bias"]).pin_memory()
+        hosts, devs = (hA, hB, hb), (prob.A, prob.B, prob.bias)
+    else:
+        hx = codes_to(torch, h["x"], wl.dtype, "cpu", pin=True)
+        hw = codes_to(torch, h["w"], wl.dtype, "cpu", pin=True)
+        hb = torch.from_numpy(h["bias"]).pin_memory()
+        hosts, devs = (hx, hw, hb), (prob.x, prob.w, prob.bias)
+    hout = torch.empty(prob.out.shape, dtype=prob.out.dtype).pin_memory()
+
+    def step():
+        for src, dst in zip(hosts, devs):
+            dst.copy_(src, non_blocking=True)
+        prob.run("fused")
+        hout.copy_(prob.out, non_blocking=True)
+
+    steps = max(5, args.steps // 5)
+    for _ in range(3):
+        step()
+    barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = start.elapsed_time(end) / steps
+    if dist is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in hosts)
+    d2h = hout.numel() * hout.element_size()
+    return {"value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+def sweep(torch, mmact, device, stream, peaks):
+    """Every workload, fused and two-kernel split: ms, TFLOP/s, % of peak, algorithmic GB/s."""
+    out = {}
+    for wl in synth.WORKLOADS.values():
+        prob = Problem(torch, mmact, wl, device)
+        flops = workload_flops(mmact, wl)
+        nbytes = workload_bytes(mmact, wl)
+        rec = {"timing": "CUDA graph of 20 back-to-back calls, replayed 3 times"}
+        for variant in ("fused", "split"):
+            ms = time_graph(torch, lambda: prob.run(variant), 20, stream)
+            tf = flops / (ms * 1e-3) / 1e12
+            rec[variant] = {"ms": round(ms, 5), "tflops": round(tf, 2),
+                            "pct_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 2),
+                            "alg_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+        st = mmact.mmact_get_last_error()
+        rec["status"] = mmact.mmact_status_string(st)
+        out[wl.name] = rec
+        del prob
+        torch.cuda.empty_cache()
+    return out
+
+
+if __name__ == "__main__":
+    sys.exit(main())

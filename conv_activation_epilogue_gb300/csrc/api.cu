@@ -1,0 +1,434 @@
+// api.cu -- the C ABI declared in include/mmact.h: argument validation, the
+// launch planner (tile shape, persistent grid, tensor-map encoding) and the
+// per-device status word.
+//
+// Argument checks mirror the MatmulLeakyRelu walkthrough's entry-point
+// validation (an invalid value is rejected with the supported set named,
+// before anything runs): every check here happens before any launch, and a
+// failed check enqueues nothing.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "mmact.h"
+
+#define MMACT_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace mmact {
+namespace {
+
+__device__ unsigned int g_status;   // per-device kernel status word (ST_* bits)
+
+constexpr uint64_t DEFAULT_WAIT_NS = 2000000000ull;
+std::atomic<uint64_t> g_wait_ns{DEFAULT_WAIT_NS};
+std::atomic<int> g_tile_n{0};
+
+constexpr int MAX_DEVICES = 64;
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    unsigned int *status = nullptr;   // device address of g_status
+};
+DeviceInfo g_dev[MAX_DEVICES];
+std::mutex g_dev_mutex;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+mmact_status device_info(DeviceInfo **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return MMACT_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MMACT_ERR_CUDA;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_status) != cudaSuccess)
+            return MMACT_ERR_CUDA;
+        if (setup_gemm_kernels() != cudaSuccess || setup_conv_kernels() != cudaSuccess)
+            return MMACT_ERR_CUDA;
+        if (g_encode == nullptr) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return MMACT_ERR_CUDA;
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return MMACT_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int out_kind(mmact_dtype d)
+{
+    return d == MMACT_BF16 ? OUT_BF16 : (d == MMACT_F16 ? OUT_F16 : OUT_F32);
+}
+int elem_bytes(mmact_dtype d) { return d == MMACT_F32 ? 4 : 2; }
+CUtensorMapDataType tmap_type(mmact_dtype d)
+{
+    return d == MMACT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                           : (d == MMACT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+}
+
+// Tiled map over a row-major tensor given innermost-first dims (elements) and
+// the byte strides of dims 1..rank-1, with a 128-byte swizzle.
+bool encode(CUtensorMap *m, mmact_dtype dt, int rank, const void *ptr, const uint64_t *dims,
+            const uint64_t *strides_bytes, const uint32_t *box)
+{
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+    }
+    for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
+    CUresult r = g_encode(m, tmap_type(dt), (cuuint32_t)rank, const_cast<void *>(ptr), gd, gs, bx, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool valid_act(mmact_act a) { return a >= MMACT_ACT_NONE && a <= MMACT_ACT_TANH; }
+bool valid_in(mmact_dtype d) { return d == MMACT_F16 || d == MMACT_BF16; }
+bool valid_out(mmact_dtype d) { return d == MMACT_F16 || d == MMACT_BF16 || d == MMACT_F32; }
+
+constexpr int64_t MAX_DIM = (int64_t(1) << 31) - 1;
+
+// Shared by mmact_gemm and the first kernel of mmact_gemm_split.
+mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void *C, int64_t M,
+                          int64_t N, int64_t K, mmact_dtype ab, mmact_dtype cd, mmact_act act,
+                          float alpha, cudaStream_t stream)
+{
+    DeviceInfo *dev = nullptr;
+    mmact_status st = device_info(&dev);
+    if (st != MMACT_OK) return st;
+    if (K == 0) {
+        cudaError_t e = launch_bias_act(bias, C, M, N, 0, N, out_kind(cd), (int)act, alpha, stream);
+        return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
+    }
+    GemmLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const int tiles_m = (int)((M + 127) / 128);
+    int bn = g_tile_n.load();
+    if (bn == 0) {
+        // Widest tile that still gives every SM at least one tile.
+        const int64_t t256 = tiles_m * ((N + 255) / 256);
+        const int64_t t128 = tiles_m * ((N + 127) / 128);
+        bn = t256 >= dev->sm_count ? 256 : (t128 >= dev->sm_count ? 128 : 64);
+    }
+    const int tiles_n = (int)((N + bn - 1) / bn);
+    GemmArgs &a = L.args;
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.tiles_m = tiles_m;
+    a.tiles_n = tiles_n;
+    a.num_tiles = tiles_m * tiles_n;
+    a.num_kb = (int)((K + 63) / 64);
+    a.group_m = 16;
+    a.ab_bf16 = ab == MMACT_BF16 ? 1 : 0;
+    a.act = (int)act;
+    a.alpha = alpha;
+    a.bias = bias;
+    a.status = dev->status;
+    a.wait_ns = g_wait_ns.load();
+    L.tile_n = bn;
+    L.out = out_kind(cd);
+    L.grid = (int)std::min<int64_t>(a.num_tiles, dev->sm_count);
+
+    const uint64_t dA[2] = {(uint64_t)K, (uint64_t)M}, sA[1] = {(uint64_t)K * 2};
+    const uint32_t bA[2] = {64, 128};
+    const uint64_t dB[2] = {(uint64_t)N, (uint64_t)K}, sB[1] = {(uint64_t)N * 2};
+    const uint32_t bB[2] = {64, 64};
+    const int ce = elem_bytes(cd);
+    const uint64_t dC[2] = {(uint64_t)N, (uint64_t)M}, sC[1] = {(uint64_t)N * ce};
+    const uint32_t bC[2] = {(uint32_t)(128 / ce), 32};
+    if (!encode(&L.tmA, ab, 2, A, dA, sA, bA) || !encode(&L.tmB, ab, 2, B, dB, sB, bB) ||
+        !encode(&L.tmC, cd, 2, C, dC, sC, bC))
+        return MMACT_ERR_CUDA;
+    return launch_gemm(L, stream) == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
+}
+
+mmact_status gemm_check(const void *A, const void *B, const float *bias, const void *C, int64_t M,
+                        int64_t N, int64_t K, mmact_dtype ab, mmact_dtype cd, mmact_act act)
+{
+    if (A == nullptr || B == nullptr || C == nullptr) return MMACT_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || M > MAX_DIM || N > MAX_DIM || K > MAX_DIM)
+        return MMACT_ERR_INVALID_ARG;
+    if (!valid_in(ab) || !valid_out(cd) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
+    if (bias != nullptr && !aligned4(bias)) return MMACT_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return MMACT_ERR_UNSUPPORTED;
+    if (K % 8 != 0 || N % 8 != 0) return MMACT_ERR_UNSUPPORTED;
+    return MMACT_OK;
+}
+
+struct ConvGeom {
+    int64_t Ho, Wo;
+};
+
+mmact_status conv_geom(int64_t H, int64_t W, int64_t kh, int64_t kw, const int32_t *st,
+                       const int32_t *pd, const int32_t *dl, ConvGeom *g)
+{
+    if (st == nullptr || pd == nullptr || dl == nullptr) return MMACT_ERR_INVALID_ARG;
+    if (H < 0 || W < 0 || kh <= 0 || kw <= 0) return MMACT_ERR_INVALID_ARG;
+    if (st[0] <= 0 || st[1] <= 0 || dl[0] <= 0 || dl[1] <= 0) return MMACT_ERR_INVALID_ARG;
+    if (pd[0] < 0 || pd[1] < 0 || pd[2] < 0 || pd[3] < 0) return MMACT_ERR_INVALID_ARG;
+    const int64_t sh = H + pd[0] + pd[1] - (int64_t)dl[0] * (kh - 1) - 1;
+    const int64_t sw = W + pd[2] + pd[3] - (int64_t)dl[1] * (kw - 1) - 1;
+    if (sh < 0 || sw < 0) return MMACT_ERR_INVALID_ARG;
+    g->Ho = sh / st[0] + 1;
+    g->Wo = sw / st[1] + 1;
+    return MMACT_OK;
+}
+
+mmact_status conv_check(const void *x, const void *w, const float *bias, const void *y, int64_t N,
+                        int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
+                        const int32_t *st, const int32_t *pd, const int32_t *dl, mmact_dtype in,
+                        mmact_dtype out, mmact_act act, ConvGeom *g)
+{
+    if (x == nullptr || w == nullptr || y == nullptr) return MMACT_ERR_INVALID_ARG;
+    if (N < 0 || C < 0 || Co < 0) return MMACT_ERR_INVALID_ARG;
+    if (!valid_in(in) || !valid_out(out) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
+    mmact_status s = conv_geom(H, W, kh, kw, st, pd, dl, g);
+    if (s != MMACT_OK) return s;
+    if (bias != nullptr && !aligned4(bias)) return MMACT_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return MMACT_ERR_UNSUPPORTED;
+    // every index the kernel forms fits in 32 bits per image / 64 bits overall
+    if (C * H * W > MAX_DIM || Co * g->Ho * g->Wo > MAX_DIM || C * kh * kw > MAX_DIM ||
+        N > MAX_DIM || H > MAX_DIM || W > MAX_DIM)
+        return MMACT_ERR_UNSUPPORTED;
+    return MMACT_OK;
+}
+
+mmact_status conv_enqueue(const void *x, const void *w, const float *bias, void *y, int64_t N,
+                          int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
+                          const int32_t *st, const int32_t *pd, const int32_t *dl, const ConvGeom &g,
+                          mmact_dtype in, mmact_dtype out, mmact_act act, float alpha,
+                          cudaStream_t stream)
+{
+    DeviceInfo *dev = nullptr;
+    mmact_status s = device_info(&dev);
+    if (s != MMACT_OK) return s;
+    const int64_t P = g.Ho * g.Wo;
+    if (N == 0 || Co == 0 || P == 0) return MMACT_OK;
+    if (C == 0) {
+        cudaError_t e = launch_bias_act(bias, y, N * Co, P, 1, Co, out_kind(out), (int)act, alpha, stream);
+        return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
+    }
+    ConvLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    ConvArgs &a = L.args;
+    a.Nb = (int)N;
+    a.C = (int)C;
+    a.H = (int)H;
+    a.W = (int)W;
+    a.Co = (int)Co;
+    a.kh = (int)kh;
+    a.kw = (int)kw;
+    a.sh = st[0];
+    a.sw = st[1];
+    a.pt = pd[0];
+    a.pl = pd[2];
+    a.dh = dl[0];
+    a.dw = dl[1];
+    a.Ho = (int)g.Ho;
+    a.Wo = (int)g.Wo;
+    a.P = (int)P;
+    a.K = (int)(C * kh * kw);
+    a.tiles_co = (int)((Co + 127) / 128);
+    a.tiles_p = (int)((P + 127) / 128);
+    a.num_tiles = (int)(N * a.tiles_co * a.tiles_p);
+    a.num_kb = (a.K + 63) / 64;
+    a.ab_bf16 = in == MMACT_BF16 ? 1 : 0;
+    a.act = (int)act;
+    a.alpha = alpha;
+    a.out_elem_bytes = elem_bytes(out);
+    a.x = static_cast<const uint16_t *>(x);
+    a.w = static_cast<const uint16_t *>(w);
+    a.bias = bias;
+    a.y = y;
+    a.status = dev->status;
+    a.wait_ns = g_wait_ns.load();
+    a.a_tma = (a.K % 8 == 0) ? 1 : 0;
+    a.y_tma = ((P * a.out_elem_bytes) % 16 == 0) ? 1 : 0;
+    L.out = out_kind(out);
+    L.grid = (int)std::min<int64_t>(a.num_tiles, dev->sm_count);
+    if (a.a_tma) {
+        const uint64_t d[2] = {(uint64_t)a.K, (uint64_t)Co}, sb[1] = {(uint64_t)a.K * 2};
+        const uint32_t bx[2] = {64, 128};
+        if (!encode(&L.tmW, in, 2, w, d, sb, bx)) return MMACT_ERR_CUDA;
+    }
+    if (a.y_tma) {
+        const int e = a.out_elem_bytes;
+        const uint64_t d[3] = {(uint64_t)P, (uint64_t)Co, (uint64_t)N};
+        const uint64_t sb[2] = {(uint64_t)P * e, (uint64_t)Co * P * e};
+        const uint32_t bx[3] = {(uint32_t)(128 / e), 32, 1};
+        if (!encode(&L.tmY, out, 3, y, d, sb, bx)) return MMACT_ERR_CUDA;
+    }
+    return launch_conv(L, stream) == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
+}
+
+int act_grid(const DeviceInfo *dev) { return dev->sm_count * 8; }
+
+}  // namespace
+}  // namespace mmact
+
+using namespace mmact;
+
+MMACT_EXPORT mmact_status mmact_gemm(const void *A, const void *B, const float *bias, void *C,
+                                     int64_t M, int64_t N, int64_t K, mmact_dtype ab_dtype,
+                                     mmact_dtype c_dtype, mmact_act act, float alpha, void *stream)
+{
+    mmact_status s = gemm_check(A, B, bias, C, M, N, K, ab_dtype, c_dtype, act);
+    if (s != MMACT_OK) return s;
+    if (M == 0 || N == 0) return MMACT_OK;
+    return gemm_enqueue(A, B, bias, C, M, N, K, ab_dtype, c_dtype, act, alpha,
+                        static_cast<cudaStream_t>(stream));
+}
+
+MMACT_EXPORT mmact_status mmact_gemm_split(const void *A, const void *B, const float *bias, void *C,
+                                           int64_t M, int64_t N, int64_t K, mmact_dtype ab_dtype,
+                                           mmact_dtype c_dtype, mmact_act act, float alpha,
+                                           float *workspace, void *stream)
+{
+    mmact_status s = gemm_check(A, B, bias, C, M, N, K, ab_dtype, c_dtype, act);
+    if (s != MMACT_OK) return s;
+    if (workspace == nullptr) return MMACT_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return MMACT_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return MMACT_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = gemm_enqueue(A, B, bias, workspace, M, N, K, ab_dtype, MMACT_F32, MMACT_ACT_NONE, 0.0f, st);
+    if (s != MMACT_OK) return s;
+    DeviceInfo *dev = nullptr;
+    if ((s = device_info(&dev)) != MMACT_OK) return s;
+    return launch_act(workspace, C, M * N, out_kind(c_dtype), (int)act, alpha, act_grid(dev), st) ==
+                   cudaSuccess
+               ? MMACT_OK
+               : MMACT_ERR_CUDA;
+}
+
+MMACT_EXPORT mmact_status mmact_conv2d(const void *x, const void *w, const float *bias, void *y,
+                                       int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co,
+                                       int64_t kh, int64_t kw, const int32_t strides[2],
+                                       const int32_t pads[4], const int32_t dilations[2],
+                                       mmact_dtype in_dtype, mmact_dtype out_dtype, mmact_act act,
+                                       float alpha, void *stream)
+{
+    ConvGeom g;
+    mmact_status s = conv_check(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations,
+                                in_dtype, out_dtype, act, &g);
+    if (s != MMACT_OK) return s;
+    return conv_enqueue(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations, g, in_dtype,
+                        out_dtype, act, alpha, static_cast<cudaStream_t>(stream));
+}
+
+MMACT_EXPORT mmact_status mmact_conv2d_split(const void *x, const void *w, const float *bias,
+                                             void *y, int64_t N, int64_t C, int64_t H, int64_t W,
+                                             int64_t Co, int64_t kh, int64_t kw,
+                                             const int32_t strides[2], const int32_t pads[4],
+                                             const int32_t dilations[2], mmact_dtype in_dtype,
+                                             mmact_dtype out_dtype, mmact_act act, float alpha,
+                                             float *workspace, void *stream)
+{
+    ConvGeom g;
+    mmact_status s = conv_check(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations,
+                                in_dtype, out_dtype, act, &g);
+    if (s != MMACT_OK) return s;
+    if (workspace == nullptr) return MMACT_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return MMACT_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = conv_enqueue(x, w, bias, workspace, N, C, H, W, Co, kh, kw, strides, pads, dilations, g,
+                     in_dtype, MMACT_F32, MMACT_ACT_NONE, 0.0f, st);
+    if (s != MMACT_OK) return s;
+    DeviceInfo *dev = nullptr;
+    if ((s = device_info(&dev)) != MMACT_OK) return s;
+    return launch_act(workspace, y, N * Co * g.Ho * g.Wo, out_kind(out_dtype), (int)act, alpha,
+                      act_grid(dev), st) == cudaSuccess
+               ? MMACT_OK
+               : MMACT_ERR_CUDA;
+}
+
+MMACT_EXPORT mmact_status mmact_conv2d_out_shape(int64_t H, int64_t W, int64_t kh, int64_t kw,
+                                                 const int32_t strides[2], const int32_t pads[4],
+                                                 const int32_t dilations[2], int64_t *Ho,
+                                                 int64_t *Wo)
+{
+    if (Ho == nullptr || Wo == nullptr) return MMACT_ERR_INVALID_ARG;
+    ConvGeom g;
+    mmact_status s = conv_geom(H, W, kh, kw, strides, pads, dilations, &g);
+    if (s != MMACT_OK) return s;
+    *Ho = g.Ho;
+    *Wo = g.Wo;
+    return MMACT_OK;
+}
+
+MMACT_EXPORT mmact_status mmact_get_last_error(void *stream)
+{
+    DeviceInfo *dev = nullptr;
+    mmact_status s = device_info(&dev);
+    if (s != MMACT_OK) return s;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MMACT_ERR_CUDA;
+    unsigned int word = 0;
+    const unsigned int zero = 0;
+    if (cudaMemcpy(&word, dev->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return MMACT_ERR_CUDA;
+    if (word & ST_TIMEOUT) return MMACT_ERR_TIMEOUT;
+    if (word != 0) return MMACT_ERR_CUDA;
+    return MMACT_OK;
+}
+
+MMACT_EXPORT void mmact_set_wait_timeout_ns(uint64_t ns)
+{
+    g_wait_ns.store(ns == 0 ? DEFAULT_WAIT_NS : ns);
+}
+
+MMACT_EXPORT mmact_status mmact_selftest_wait_timeout(uint64_t timeout_ns, void *stream)
+{
+    DeviceInfo *dev = nullptr;
+    mmact_status s = device_info(&dev);
+    if (s != MMACT_OK) return s;
+    return launch_wait_selftest(dev->status, timeout_ns, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? MMACT_OK
+               : MMACT_ERR_CUDA;
+}
+
+MMACT_EXPORT mmact_status mmact_set_gemm_tile_n(int tile_n)
+{
+    if (tile_n != 0 && tile_n != 64 && tile_n != 128 && tile_n != 256) return MMACT_ERR_INVALID_ARG;
+    g_tile_n.store(tile_n);
+    return MMACT_OK;
+}
+
+MMACT_EXPORT const char *mmact_status_string(mmact_status status)
+{
+    switch (status) {
+    case MMACT_OK: return "MMACT_OK";
+    case MMACT_ERR_INVALID_ARG: return "MMACT_ERR_INVALID_ARG: invalid argument";
+    case MMACT_ERR_UNSUPPORTED: return "MMACT_ERR_UNSUPPORTED: alignment or dtype combination not supported";
+    case MMACT_ERR_CUDA: return "MMACT_ERR_CUDA: a CUDA call failed";
+    case MMACT_ERR_TIMEOUT: return "MMACT_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
+    default: return "unknown mmact_status";
+    }
+}
+
+MMACT_EXPORT int mmact_version(void) { return 1; }

@@ -1,0 +1,191 @@
+// common.cuh -- device code shared by the fused GEMM and implicit-GEMM conv
+// kernels: the activation functions, output packing, the tcgen05 MMA issuer
+// role and the TMEM -> registers -> swizzled shared memory epilogue unit.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace mmact {
+
+enum : int { ACT_NONE = 0, ACT_RELU = 1, ACT_LEAKY = 2, ACT_TANH = 3 };
+enum : int { OUT_F32 = 0, OUT_F16 = 1, OUT_BF16 = 2 };
+
+// Bits of the per-device status word.
+enum : unsigned { ST_TIMEOUT = 1u, ST_SMEM_ALIGN = 2u };
+
+constexpr uint64_t DRAIN_NS = 1000000000ull;   // bound on end-of-kernel drains
+
+// tanh(z) as the ratio of exponentials (e^z - e^-z) / (e^z + e^-z), with
+// numerator and denominator multiplied by e^-|z| so that nothing overflows:
+// tanh(|z|) = (1 - e^{-2|z|}) / (1 + e^{-2|z|}), sign restored last.
+__device__ __forceinline__ float tanh_f32(float z)
+{
+    const float e = __expf(-2.0f * fabsf(z));
+    return copysignf(__fdividef(1.0f - e, 1.0f + e), z);
+}
+
+template <int ACT>
+__device__ __forceinline__ float act_f32(float z, float alpha)
+{
+    if constexpr (ACT == ACT_RELU) return z > 0.0f ? z : 0.0f;
+    else if constexpr (ACT == ACT_LEAKY) return z > 0.0f ? z : alpha * z;
+    else if constexpr (ACT == ACT_TANH) return tanh_f32(z);
+    else return z;
+}
+
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    if constexpr (OUT == OUT_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+// Shared-memory addresses of the pipeline's barriers and flags.
+struct Pipe {
+    uint32_t full0, empty0;      // operand ring: barrier s at +8*s
+    uint32_t tfull0, tempty0;    // accumulator ring (2 buffers)
+    uint32_t drain;
+    uint32_t tmem;               // TMEM base address of the accumulators
+    volatile uint32_t *abort;    // set when any role gives up
+    unsigned int *status;        // device status word
+    uint64_t wait_ns;
+};
+
+__device__ __forceinline__ void pipe_fail(const Pipe &pp)
+{
+    *pp.abort = 1u;
+    atomicOr(pp.status, ST_TIMEOUT);
+}
+
+__device__ __forceinline__ bool pipe_wait(const Pipe &pp, uint32_t bar, uint32_t parity)
+{
+    return ptx::mbar_wait_bounded(bar, parity, pp.wait_ns, pp.abort);
+}
+
+// The MMA issuer (one thread).  For every tile of this CTA it waits for a free
+// accumulator buffer, then for each K block waits for the operand stage,
+// issues BK/16 tcgen05.mma instructions and commits the stage back to the
+// producer; the finished accumulator is committed to the epilogue.
+//   A stage: [128 rows x 64 K] K-major, 128-byte swizzle (rows 128 B apart,
+//            8-row groups 1024 B apart); the K step of 16 moves 32 bytes.
+//   B stage: [64 K x BN] MN-major, 128-byte swizzle, BN/64 column chunks of
+//            64 K rows x 128 B each (chunk stride 8192 B); the K step of 16
+//            moves 16 rows = 2048 bytes.
+template <int BN, int STAGES>
+__device__ void mma_role(const Pipe &pp, uint32_t sA, uint32_t sB, int num_tiles, int num_kb,
+                         uint32_t idesc)
+{
+    constexpr uint32_t A_BYTES = 128 * 64 * 2, B_BYTES = 64 * BN * 2;
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        if (!pipe_wait(pp, pp.tempty0 + 8 * acc, acc_phase ^ 1u)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t d = pp.tmem + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+            if (!pipe_wait(pp, pp.full0 + 8 * stage, phase)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t a0 = sA + stage * A_BYTES, b0 = sB + stage * B_BYTES;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = ptx::smem_desc(a0 + 32u * k, 16u, 1024u, ptx::SWIZZLE_128B);
+                const uint64_t bd = ptx::smem_desc(b0 + 2048u * k, 8192u, 1024u, ptx::SWIZZLE_128B);
+                ptx::mma_f16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(pp.empty0 + 8 * stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::mma_commit(pp.tfull0 + 8 * acc);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) pipe_fail(pp);
+    // Every MMA this thread issued must finish before TMEM is released.
+    ptx::mma_commit(pp.drain);
+    ptx::mbar_wait_bounded(pp.drain, 0, DRAIN_NS, nullptr);
+}
+
+// One epilogue unit: 32 rows (this warp's TMEM lane quarter) x one 128-byte
+// output row segment (32 fp32 or 64 16-bit columns).  Loads the fp32
+// accumulators from TMEM, adds the fp32 bias (per column from global memory
+// `bias_col[0..nvalid)`, zero beyond it or when null; or the per-row `brow`),
+// applies the activation in fp32, converts, and writes the row into a
+// 32 x 128 B shared buffer in the 128-byte swizzled order a TMA store expects
+// (16-byte chunk c of row r lands at chunk c ^ (r & 7)).
+template <int OUT, int ACT, bool BIAS_ROW>
+__device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, int nvalid,
+                                         float brow, float alpha, uint32_t buf, int lane)
+{
+    constexpr int COLS = OUT == OUT_F32 ? 32 : 64;
+    uint32_t r0[32];
+    uint32_t r1[32];
+    ptx::tmem_ld32(taddr, r0);
+    if constexpr (OUT != OUT_F32) ptx::tmem_ld32(taddr + 32, r1);
+    float bc[COLS];
+#pragma unroll
+    for (int j = 0; j < COLS; ++j)
+        bc[j] = BIAS_ROW ? brow : ((bias_col != nullptr && j < nvalid) ? __ldg(bias_col + j) : 0.0f);
+    ptx::tmem_ld_wait(r0);
+    if constexpr (OUT != OUT_F32) ptx::tmem_ld_wait(r1);
+    const uint32_t row = buf + (uint32_t)lane * 128u;
+    const uint32_t sw = (uint32_t)(lane & 7);
+    if constexpr (OUT == OUT_F32) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int col = 4 * c + e;
+                v[e] = act_f32<ACT>(__uint_as_float(r0[col]) + bc[col], alpha);
+            }
+            ptx::st_shared_v4(row + (((uint32_t)c ^ sw) << 4), __float_as_uint(v[0]),
+                              __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int col = 8 * c + 2 * e;
+                const uint32_t ua = col < 32 ? r0[col] : r1[col - 32];
+                const uint32_t ub = col + 1 < 32 ? r0[col + 1] : r1[col + 1 - 32];
+                w[e] = pack2<OUT>(act_f32<ACT>(__uint_as_float(ua) + bc[col], alpha),
+                                  act_f32<ACT>(__uint_as_float(ub) + bc[col + 1], alpha));
+            }
+            ptx::st_shared_v4(row + (((uint32_t)c ^ sw) << 4), w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+template <int OUT, bool BIAS_ROW>
+__device__ __forceinline__ void epi_unit_dispatch(int act, uint32_t taddr, const float *bias_col,
+                                                  int nvalid, float brow, float alpha, uint32_t buf,
+                                                  int lane)
+{
+    switch (act) {
+    case ACT_RELU:
+        epi_unit<OUT, ACT_RELU, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        break;
+    case ACT_LEAKY:
+        epi_unit<OUT, ACT_LEAKY, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        break;
+    case ACT_TANH:
+        epi_unit<OUT, ACT_TANH, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        break;
+    default:
+        epi_unit<OUT, ACT_NONE, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        break;
+    }
+}
+
+}  // namespace mmact

@@ -1,0 +1,312 @@
+// conv.cu -- persistent, warp-specialised implicit-GEMM conv2d (NCHW) with the
+// fused bias + activation epilogue:  y = act(conv2d(x, w) + bias).
+//
+// "multimodal-ops Fused ConvTanh" article, section on how the two kernels
+// split the work: the convolution is an implicit GEMM whose A operand is the
+// filter [Co x K] (K = Ci*kh*kw in the filter's own (ci, r, q) order) and whose
+// B operand is the input features [K x Ho*Wo], so each image's result
+// [Co, Ho*Wo] is already NCHW.  Per image n the GEMM view is
+//
+//   y[n][co][p] = act(bias[co] + sum_k w[co][k] * X_n[k][p]),
+//   X_n[(ci,r,q)][(oh,ow)] = x[n][ci][oh*sh - pt + r*dh][ow*sw - pl + q*dw]
+//                            (0 outside the image),
+//
+// with X_n never materialised: producer warps gather each [64 K x 128 pixel]
+// B tile straight from x into shared memory, in the MN-major 128-byte
+// swizzled layout tcgen05.mma reads (the im2col addresses for stride, pad and
+// dilation are generated on the fly).  The filter tile [128 co x 64 K] comes
+// by TMA when its row pitch allows (K * 2 bytes a multiple of 16), else it is
+// gathered too.  The MMA issuer and the epilogue are the GEMM kernel's; the
+// epilogue adds bias per output channel (per accumulator row) and stores each
+// 32-channel x 64-pixel block with a 3-D TMA store into y viewed as
+// [N][Co][Ho*Wo] (or with plain stores when y's row pitch is not 16-byte
+// aligned).  The article's stride-2 odd/even column split is not needed:
+// address generation handles any stride.
+//
+// Warps: 0 filter TMA, 1 TMEM + MMA, 2..5 epilogue, 6..9 B-tile gather.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mmact {
+
+struct ConvCfg {
+    static constexpr int BM = 128, BN = 128, BK = 64;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BK * BN * 2;
+    static constexpr int STAGES = 6;
+    static constexpr int EPI_BYTES = 4 * 2 * 4096;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16;
+    static constexpr int THREADS = 320;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// tile -> (image, pixel block, channel block); channel blocks vary fastest so
+// CTAs running side by side share the same input pixels in L2.
+__device__ __forceinline__ void conv_tile(int t, const ConvArgs &p, int &n, int &pb, int &cb)
+{
+    cb = t % p.tiles_co;
+    const int r = t / p.tiles_co;
+    pb = r % p.tiles_p;
+    n = r / p.tiles_p;
+}
+
+// Byte offset of element (k, j) inside an MN-major 128B-swizzled [64 x 128] tile.
+__device__ __forceinline__ uint32_t b_tile_offset(int k, int j)
+{
+    return (uint32_t)((j >> 6) * 8192 + k * 128 + ((((j >> 3) & 7) ^ (k & 7)) << 4) + ((j & 7) << 1));
+}
+
+// Byte offset of element (m, k) inside a K-major 128B-swizzled [128 x 64] tile.
+__device__ __forceinline__ uint32_t a_tile_offset(int m, int k)
+{
+    return (uint32_t)(m * 128 + ((((k >> 3) & 7) ^ (m & 7)) << 4) + ((k & 7) << 1));
+}
+
+template <int OUT>
+__global__ void __launch_bounds__(ConvCfg::THREADS, 1)
+    conv_act_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmY,
+                    const ConvArgs p)
+{
+    using Cfg = ConvCfg;
+    constexpr int STAGES = Cfg::STAGES, BN = Cfg::BN;
+    constexpr int COLS = OUT == OUT_F32 ? 32 : 64;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const uint32_t base = ptx::smem_addr(smem);
+    if (base & 1023u) {
+        if (threadIdx.x == 0) atomicOr(p.status, ST_SMEM_ALIGN);
+        return;
+    }
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
+    Pipe pp;
+    pp.full0 = base + Cfg::OFF_BAR;
+    pp.empty0 = pp.full0 + 8 * STAGES;
+    pp.tfull0 = pp.empty0 + 8 * STAGES;
+    pp.tempty0 = pp.tfull0 + 16;
+    pp.drain = pp.tempty0 + 16;
+    pp.abort = misc + 1;
+    pp.status = p.status;
+    pp.wait_ns = p.wait_ns;
+
+    if (threadIdx.x == 0) {
+        // full: the 4 gather warps, plus the filter TMA producer when it is used
+        const uint32_t full_count = p.a_tma ? 5u : 4u;
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(pp.full0 + 8 * s, full_count);
+            ptx::mbar_init(pp.empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(pp.tfull0 + 8 * a, 1);
+            ptx::mbar_init(pp.tempty0 + 8 * a, 4);
+        }
+        ptx::mbar_init(pp.drain, 1);
+        misc[1] = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(base + Cfg::OFF_MISC, Cfg::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    pp.tmem = misc[0];
+
+    const uint32_t sA = base + Cfg::OFF_A, sB = base + Cfg::OFF_B;
+
+    if (warp == 0) {
+        if (lane == 0 && p.a_tma) {
+            // ---------------------------------------------- filter producer --
+            ptx::prefetch_tensormap(&tmW);
+            uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+                int n, pb, cb;
+                conv_tile(t, p, n, pb, cb);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u)) { ok = false; break; }
+                    const uint32_t fb = pp.full0 + 8 * stage;
+                    ptx::mbar_arrive_expect_tx(fb, Cfg::A_BYTES);
+                    ptx::tma_load_2d(sA + stage * Cfg::A_BYTES, &tmW, fb, kb * 64, cb * 128);
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) pipe_fail(pp);
+            for (int s = 0; s < STAGES; ++s)
+                if (issued & (1u << s))
+                    ptx::mbar_wait_bounded(pp.full0 + 8 * s, (last_par >> s) & 1u, DRAIN_NS, nullptr);
+        }
+    } else if (warp == 1) {
+        if (lane == 0)
+            mma_role<BN, STAGES>(pp, sA, sB, p.num_tiles, p.num_kb,
+                                 ptx::idesc_f16(p.ab_bf16 != 0, false, true, 128, BN));
+    } else if (warp >= 6) {
+        // ---------------------------------------------------- B-tile gather --
+        const int j = threadIdx.x - 192;              // this thread's pixel column, 0..127
+        const int64_t HW = (int64_t)p.H * p.W;
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+            int n, pb, cb;
+            conv_tile(t, p, n, pb, cb);
+            const int pix = pb * BN + j;
+            const bool pvalid = pix < p.P;
+            const int oh = pvalid ? pix / p.Wo : 0;
+            const int ow = pvalid ? pix - oh * p.Wo : 0;
+            const int ih0 = oh * p.sh - p.pt, iw0 = ow * p.sw - p.pl;
+            const uint16_t *xn = p.x + (int64_t)n * p.C * HW;
+            const int co_rows = p.Co - cb * 128;      // filter rows valid in this tile (gathered A)
+            // (ci, r, q) of the next K index, advanced one step per element
+            int ci = 0, r = 0, q = 0, k = 0;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                uint32_t go = 1;
+                if (lane == 0) go = pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u) ? 1u : 0u;
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) { ok = false; break; }
+                const uint32_t bt = sB + stage * Cfg::B_BYTES;
+#pragma unroll 4
+                for (int kl = 0; kl < 64; ++kl) {
+                    uint16_t v = 0;
+                    if (k < p.K) {
+                        const int ih = ih0 + r * p.dh, iw = iw0 + q * p.dw;
+                        if (pvalid && (unsigned)ih < (unsigned)p.H && (unsigned)iw < (unsigned)p.W)
+                            v = __ldg(xn + (int64_t)ci * HW + (int64_t)ih * p.W + iw);
+                    }
+                    ptx::st_shared_u16(bt + b_tile_offset(kl, j), v);
+                    ++k;
+                    if (++q == p.kw) {
+                        q = 0;
+                        if (++r == p.kh) { r = 0; ++ci; }
+                    }
+                }
+                if (!p.a_tma) {
+                    // filter tile rows m = j: w[cb*128 + m][kb*64 .. +64)
+                    const uint32_t at = sA + stage * Cfg::A_BYTES;
+                    const uint16_t *wr = p.w + (int64_t)(cb * 128 + j) * p.K;
+                    for (int kl = 0; kl < 64; ++kl) {
+                        const int kk = kb * 64 + kl;
+                        const uint16_t v = (j < co_rows && kk < p.K) ? __ldg(wr + kk) : (uint16_t)0;
+                        ptx::st_shared_u16(at + a_tile_offset(j, kl), v);
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(pp.full0 + 8 * stage);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!ok) pipe_fail(pp);
+    } else {
+        // -------------------------------------------------------- epilogue --
+        const int qd = warp & 3;
+        const uint32_t my_buf = base + Cfg::OFF_EPI + (uint32_t)qd * 8192u;
+        uint32_t acc = 0, acc_phase = 0;
+        uint32_t units = 0;      // running count: picks the staging buffer
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+            int n, pb, cb;
+            conv_tile(t, p, n, pb, cb);
+            const int co_row0 = cb * 128 + qd * 32;
+            const int co = co_row0 + lane;
+            const float brow = (p.bias != nullptr && co < p.Co) ? __ldg(p.bias + co) : 0.0f;
+            uint32_t got = 1;
+            if (lane == 0) got = pipe_wait(pp, pp.tfull0 + 8 * acc, acc_phase) ? 1u : 0u;
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t tbase = pp.tmem + ((uint32_t)(qd * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int u = 0; u < BN / COLS; ++u) {
+                const uint32_t buf = my_buf + (units++ & 1u) * 4096u;
+                const int pix0 = pb * BN + u * COLS;
+                if (lane == 0) ptx::bulk_wait_read<1>();
+                __syncwarp();
+                epi_unit_dispatch<OUT, true>(p.act, tbase + u * COLS, nullptr, 0, brow, p.alpha, buf,
+                                             lane);
+                if (p.y_tma) {
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && co_row0 < p.Co && pix0 < p.P) {
+                        ptx::tma_store_3d(&tmY, buf, pix0, co_row0, n);
+                        ptx::bulk_commit();
+                    }
+                } else if (co < p.Co) {
+                    // plain stores of this thread's row segment, read back from its swizzled row
+                    const uint8_t *row = smem + (buf - base) + lane * 128;
+                    uint8_t *dst = reinterpret_cast<uint8_t *>(p.y) +
+                                   (((int64_t)n * p.Co + co) * p.P + pix0) * p.out_elem_bytes;
+                    const int nvalid = min(COLS, p.P - pix0);
+                    for (int e = 0; e < nvalid; ++e) {
+                        const int byte = e * p.out_elem_bytes;
+                        const int chunk = (byte >> 4) ^ (lane & 7);
+                        const uint8_t *src = row + chunk * 16 + (byte & 15);
+                        if (p.out_elem_bytes == 4)
+                            *reinterpret_cast<uint32_t *>(dst + byte) = *reinterpret_cast<const uint32_t *>(src);
+                        else
+                            *reinterpret_cast<uint16_t *>(dst + byte) = *reinterpret_cast<const uint16_t *>(src);
+                    }
+                    __syncwarp();
+                } else {
+                    __syncwarp();
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(pp.tempty0 + 8 * acc);
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (!ok) pipe_fail(pp);
+        if (lane == 0) ptx::bulk_wait<0>();
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(pp.tmem, Cfg::TMEM_COLS);
+    }
+}
+
+template <int OUT>
+static cudaError_t launch_conv_t(const ConvLaunch &L, cudaStream_t stream)
+{
+    conv_act_kernel<OUT><<<L.grid, ConvCfg::THREADS, ConvCfg::SMEM_BYTES, stream>>>(L.tmW, L.tmY,
+                                                                                    L.args);
+    return cudaGetLastError();
+}
+
+cudaError_t setup_conv_kernels()
+{
+    cudaError_t e = cudaFuncSetAttribute(conv_act_kernel<OUT_BF16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         ConvCfg::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(conv_act_kernel<OUT_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ConvCfg::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(conv_act_kernel<OUT_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ConvCfg::SMEM_BYTES);
+    return e;
+}
+
+cudaError_t launch_conv(const ConvLaunch &L, cudaStream_t stream)
+{
+    if (L.out == OUT_BF16) return launch_conv_t<OUT_BF16>(L, stream);
+    if (L.out == OUT_F16) return launch_conv_t<OUT_F16>(L, stream);
+    if (L.out == OUT_F32) return launch_conv_t<OUT_F32>(L, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace mmact

@@ -1,0 +1,74 @@
+// kernels.h -- host-side view of the kernels: argument blocks and launchers.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mmact {
+
+struct GemmArgs {
+    int M, N, K;
+    int tiles_m, tiles_n, num_tiles, num_kb;
+    int group_m;         // M tiles that share one sweep over N (L2 reuse)
+    int ab_bf16;         // 1: bf16 operands, 0: fp16
+    int act;             // ACT_*
+    float alpha;
+    const float *bias;   // [N] or null
+    unsigned int *status;
+    unsigned long long wait_ns;
+};
+
+struct GemmLaunch {
+    CUtensorMap tmA, tmB, tmC;
+    GemmArgs args;
+    int tile_n;          // 64, 128 or 256
+    int out;             // OUT_*
+    int grid;
+};
+
+struct ConvArgs {
+    int Nb, C, H, W, Co, kh, kw;
+    int sh, sw, pt, pl, dh, dw;
+    int Ho, Wo, P;       // P = Ho * Wo
+    int K;               // C * kh * kw
+    int tiles_co, tiles_p, num_tiles, num_kb;
+    int ab_bf16;
+    int act;
+    float alpha;
+    int a_tma;           // 1: filter tiles by TMA, 0: gathered by the producer warps
+    int y_tma;           // 1: output tiles by TMA store, 0: direct global stores
+    int out_elem_bytes;
+    const uint16_t *x;
+    const uint16_t *w;
+    const float *bias;
+    void *y;
+    unsigned int *status;
+    unsigned long long wait_ns;
+};
+
+struct ConvLaunch {
+    CUtensorMap tmW, tmY;
+    ConvArgs args;
+    int out;
+    int grid;
+};
+
+// One-time per-device set-up (dynamic shared-memory opt-in of every instance);
+// must run with the device current, before the first launch on it.
+cudaError_t setup_gemm_kernels();
+cudaError_t setup_conv_kernels();
+cudaError_t launch_gemm(const GemmLaunch &L, cudaStream_t stream);
+cudaError_t launch_conv(const ConvLaunch &L, cudaStream_t stream);
+// out[i] = act(ws[i]) for i < count (ws fp32, out of dtype `out`).
+cudaError_t launch_act(const float *ws, void *out, int64_t count, int out_kind, int act,
+                       float alpha, int grid, cudaStream_t stream);
+// out[r][c] = act(bias[c]) (bias may be null) for an [rows x cols] output;
+// with per_row != 0 the bias runs along rows: out[r][c] = act(bias[r % bias_len]).
+cudaError_t launch_bias_act(const float *bias, void *out, int64_t rows, int64_t cols, int per_row,
+                            int64_t bias_len, int out_kind, int act, float alpha,
+                            cudaStream_t stream);
+cudaError_t launch_wait_selftest(unsigned int *status, unsigned long long timeout_ns,
+                                 cudaStream_t stream);
+
+}  // namespace mmact

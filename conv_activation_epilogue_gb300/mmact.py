@@ -1,0 +1,226 @@
+"""Thin Python binding over libmmact.so (the C ABI in include/mmact.h).
+
+Argument marshalling only: every function here checks that the torch tensors
+it is handed are CUDA, contiguous and of a supported dtype, turns them into
+raw device pointers and sizes, calls the C entry point of the same name and
+raises MmactError on a non-OK status.  All arithmetic runs in the library's
+CUDA kernels; there is no CPU path.  If the library is not built, the first
+call raises instead of falling back to anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_HERE, "libmmact.so")
+
+MMACT_OK, MMACT_ERR_INVALID_ARG, MMACT_ERR_UNSUPPORTED, MMACT_ERR_CUDA, MMACT_ERR_TIMEOUT = range(5)
+ACT = {"none": 0, "relu": 1, "leaky_relu": 2, "tanh": 3}
+DTYPE = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
+
+_lib = None
+
+# Exported C symbols, as declared in include/mmact.h.
+SYMBOLS = [
+    "mmact_gemm", "mmact_gemm_split", "mmact_conv2d", "mmact_conv2d_split",
+    "mmact_conv2d_out_shape", "mmact_get_last_error", "mmact_set_wait_timeout_ns",
+    "mmact_selftest_wait_timeout", "mmact_set_gemm_tile_n", "mmact_status_string", "mmact_version",
+]
+
+
+class MmactError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def load(path: str = LIBRARY) -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"libmmact.so not found at {path}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+    L = ctypes.CDLL(path)
+    vp, i64, i32, f32, u64, ci = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                                  ctypes.c_uint64, ctypes.c_int)
+    p_i32 = ctypes.POINTER(i32)
+    L.mmact_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, f32, vp]
+    L.mmact_gemm_split.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, f32, vp, vp]
+    conv = [vp, vp, vp, vp] + [i64] * 7 + [p_i32, p_i32, p_i32, ci, ci, ci, f32]
+    L.mmact_conv2d.argtypes = conv + [vp]
+    L.mmact_conv2d_split.argtypes = conv + [vp, vp]
+    L.mmact_conv2d_out_shape.argtypes = [i64, i64, i64, i64, p_i32, p_i32, p_i32,
+                                         ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    L.mmact_get_last_error.argtypes = [vp]
+    L.mmact_set_wait_timeout_ns.argtypes = [u64]
+    L.mmact_set_wait_timeout_ns.restype = None
+    L.mmact_selftest_wait_timeout.argtypes = [u64, vp]
+    L.mmact_set_gemm_tile_n.argtypes = [ci]
+    L.mmact_status_string.argtypes = [ci]
+    L.mmact_status_string.restype = ctypes.c_char_p
+    L.mmact_version.argtypes = []
+    for name in ("mmact_gemm", "mmact_gemm_split", "mmact_conv2d", "mmact_conv2d_split",
+                 "mmact_conv2d_out_shape", "mmact_get_last_error", "mmact_selftest_wait_timeout",
+                 "mmact_set_gemm_tile_n", "mmact_version"):
+        getattr(L, name).restype = ci
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return load().mmact_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != MMACT_OK:
+        raise MmactError(status, where)
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _dev(t: torch.Tensor, name: str, dtypes) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} dtype {t.dtype} not in {dtypes}")
+    return t.data_ptr()
+
+
+_IN = (torch.float16, torch.bfloat16)
+_OUT = (torch.float16, torch.bfloat16, torch.float32)
+
+
+def _bias_ptr(bias, n: int):
+    if bias is None:
+        return None
+    _dev(bias, "bias", (torch.float32,))
+    if bias.numel() != n:
+        raise ValueError(f"bias must have {n} elements")
+    return bias.data_ptr()
+
+
+def _gemm_args(A, B, bias, C):
+    pa = _dev(A, "A", _IN)
+    pb = _dev(B, "B", _IN)
+    pc = _dev(C, "C", _OUT)
+    if A.dim() != 2 or B.dim() != 2 or C.dim() != 2:
+        raise ValueError("A, B, C must be 2-D")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N) or B.dtype != A.dtype:
+        raise ValueError("shape/dtype mismatch: A [M,K], B [K,N], C [M,N], A and B same dtype")
+    return pa, pb, _bias_ptr(bias, N), pc, M, N, K
+
+
+def mmact_gemm(A, B, bias, C, act: str = "none", alpha: float = 0.0, stream=None) -> None:
+    """C = act(A @ B + bias) in one fused kernel (see include/mmact.h)."""
+    L = load()
+    pa, pb, pbias, pc, M, N, K = _gemm_args(A, B, bias, C)
+    _check(L.mmact_gemm(pa, pb, pbias, pc, M, N, K, DTYPE[A.dtype], DTYPE[C.dtype], ACT[act],
+                        float(alpha), _stream_handle(stream)), "mmact_gemm")
+
+
+def mmact_gemm_split(A, B, bias, C, workspace, act: str = "none", alpha: float = 0.0,
+                     stream=None) -> None:
+    """Two-kernel ablation: workspace (fp32 [M,N]) = A @ B + bias, then C = act(workspace)."""
+    L = load()
+    pa, pb, pbias, pc, M, N, K = _gemm_args(A, B, bias, C)
+    pw = _dev(workspace, "workspace", (torch.float32,))
+    if workspace.numel() < M * N:
+        raise ValueError("workspace must hold M*N fp32 elements")
+    _check(L.mmact_gemm_split(pa, pb, pbias, pc, M, N, K, DTYPE[A.dtype], DTYPE[C.dtype], ACT[act],
+                              float(alpha), pw, _stream_handle(stream)), "mmact_gemm_split")
+
+
+def _i32(vals, n):
+    vals = tuple(int(v) for v in vals)
+    if len(vals) != n:
+        raise ValueError(f"expected {n} values")
+    return (ctypes.c_int32 * n)(*vals)
+
+
+def mmact_conv2d_out_shape(H, W, kh, kw, stride, pads, dilation) -> tuple:
+    L = load()
+    ho, wo = ctypes.c_int64(), ctypes.c_int64()
+    _check(L.mmact_conv2d_out_shape(H, W, kh, kw, _i32(stride, 2), _i32(pads, 4),
+                                    _i32(dilation, 2), ctypes.byref(ho), ctypes.byref(wo)),
+           "mmact_conv2d_out_shape")
+    return ho.value, wo.value
+
+
+def _conv_args(x, w, bias, y, stride, pads, dilation):
+    px = _dev(x, "x", _IN)
+    pw = _dev(w, "w", _IN)
+    py = _dev(y, "y", _OUT)
+    if x.dim() != 4 or w.dim() != 4 or y.dim() != 4:
+        raise ValueError("x, w, y must be 4-D (NCHW / [Co,C,kh,kw])")
+    N, C, H, W = x.shape
+    Co, C2, kh, kw = w.shape
+    if C2 != C or w.dtype != x.dtype:
+        raise ValueError("w must be [Co, C, kh, kw] with x's dtype")
+    Ho, Wo = mmact_conv2d_out_shape(H, W, kh, kw, stride, pads, dilation)
+    if tuple(y.shape) != (N, Co, Ho, Wo):
+        raise ValueError(f"y must be {(N, Co, Ho, Wo)}")
+    return (px, pw, _bias_ptr(bias, Co), py, N, C, H, W, Co, kh, kw, _i32(stride, 2),
+            _i32(pads, 4), _i32(dilation, 2))
+
+
+def mmact_conv2d(x, w, bias, y, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1),
+                 act: str = "tanh", alpha: float = 0.0, stream=None) -> None:
+    """y = act(conv2d(x, w) + bias), NCHW, pads = (top, bottom, left, right)."""
+    L = load()
+    args = _conv_args(x, w, bias, y, stride, pads, dilation)
+    _check(L.mmact_conv2d(*args, DTYPE[x.dtype], DTYPE[y.dtype], ACT[act], float(alpha),
+                          _stream_handle(stream)), "mmact_conv2d")
+
+
+def mmact_conv2d_split(x, w, bias, y, workspace, stride=(1, 1), pads=(0, 0, 0, 0),
+                       dilation=(1, 1), act: str = "tanh", alpha: float = 0.0, stream=None) -> None:
+    """Two-kernel ablation of mmact_conv2d through an fp32 workspace shaped like y."""
+    L = load()
+    args = _conv_args(x, w, bias, y, stride, pads, dilation)
+    pws = _dev(workspace, "workspace", (torch.float32,))
+    if workspace.numel() < y.numel():
+        raise ValueError("workspace must hold y.numel() fp32 elements")
+    _check(L.mmact_conv2d_split(*args, DTYPE[x.dtype], DTYPE[y.dtype], ACT[act], float(alpha), pws,
+                                _stream_handle(stream)), "mmact_conv2d_split")
+
+
+def mmact_get_last_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word's verdict."""
+    return int(load().mmact_get_last_error(_stream_handle(stream)))
+
+
+def mmact_set_wait_timeout_ns(ns: int) -> None:
+    load().mmact_set_wait_timeout_ns(int(ns))
+
+
+def mmact_selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
+    _check(load().mmact_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream)),
+           "mmact_selftest_wait_timeout")
+
+
+def mmact_set_gemm_tile_n(tile_n: int) -> None:
+    _check(load().mmact_set_gemm_tile_n(int(tile_n)), "mmact_set_gemm_tile_n")
+
+
+def mmact_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def mmact_version() -> int:
+    return int(load().mmact_version())

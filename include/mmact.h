@@ -1,0 +1,189 @@
+/*
+ * mmact.h -- C ABI of the fused GEMM / implicit-GEMM conv + bias + activation
+ * library for GB300 (sm_103a).  libmmact.so exports exactly these symbols.
+ *
+ * Operations
+ *   C = act(A x B + bias)                        mmact_gemm, mmact_gemm_split
+ *     "MatmulLeakyRelu fusion walkthrough" (pyasc examples/05_matmul_leakyrelu):
+ *     overview formula C = A x B + Bias then LeakyReLU, computed in one kernel;
+ *     sample spec table (A [M,K], B [K,N] row-major and not transposed, bias
+ *     fp32 [1,N], C fp32).  ReLU: "ops-nn fused_matmul_relu" article, the
+ *     fused call on 4096^3 and its two-call fallback (matmul into a device
+ *     temporary, then relu).
+ *   y = act(conv2d(x, w, bias))                  mmact_conv2d, mmact_conv2d_split
+ *     "multimodal-ops Fused ConvTanh" article: y = tanh(conv2d(x, filter,
+ *     bias)) with strides / pads / dilations; the convolution is an implicit
+ *     GEMM whose A operand is the filter [Co x Ci*kh*kw] and whose B operand is
+ *     the input features [Ci*kh*kw x Ho*Wo], so the result is already laid out
+ *     [Co, Ho*Wo] per image (NCHW) -- section "how the two kernels split the
+ *     work".  The *_split variants are that article's two-kernel "half fusion"
+ *     (fp32 workspace in device memory, then a separate activation pass), kept
+ *     as a measured ablation.
+ *
+ * Activations (all evaluated in fp32 on the fp32 accumulator plus the fp32
+ * bias, then rounded to the output dtype with round-to-nearest-even):
+ *   MMACT_ACT_NONE        z
+ *   MMACT_ACT_RELU        z > 0 ? z : 0
+ *   MMACT_ACT_LEAKY_RELU  z > 0 ? z : alpha * z
+ *   MMACT_ACT_TANH        (e^z - e^-z) / (e^z + e^-z)
+ *
+ * Conventions for every entry point
+ *   - Tensor pointers are DEVICE pointers (cudaMalloc / torch CUDA memory) on
+ *     the current CUDA device.  The caller owns every buffer; the library
+ *     never allocates, frees or retains them.
+ *   - All tensors are dense and row-major (C order).  16-byte alignment is
+ *     required of A, B, C, x, y, w and workspace; 4-byte alignment of bias.
+ *   - bias may be NULL (treated as all zeros).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous: they validate arguments on the host,
+ *     enqueue kernels on `stream` and return.  A status other than MMACT_OK
+ *     means nothing was enqueued.
+ *   - Errors that arise inside a kernel (a bounded wait that ran out) are
+ *     recorded in a per-device status word; mmact_get_last_error() reads and
+ *     clears it.
+ *   - Thread safety: calls may come from several host threads; the only
+ *     shared state is the per-device status word and one-time kernel set-up.
+ */
+#ifndef MMACT_H
+#define MMACT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MMACT_OK = 0,
+    MMACT_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad enum, bad geometry */
+    MMACT_ERR_UNSUPPORTED = 2,   /* valid request this build does not handle (alignment, dtype pair) */
+    MMACT_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+    MMACT_ERR_TIMEOUT = 4        /* a kernel's bounded wait ran out (reported by get_last_error) */
+} mmact_status;
+
+typedef enum {
+    MMACT_ACT_NONE = 0,
+    MMACT_ACT_RELU = 1,
+    MMACT_ACT_LEAKY_RELU = 2,
+    MMACT_ACT_TANH = 3
+} mmact_act;
+
+typedef enum {
+    MMACT_F16 = 0,
+    MMACT_BF16 = 1,
+    MMACT_F32 = 2
+} mmact_dtype;
+
+/*
+ * Fused single-kernel GEMM + bias + activation:  C = act(A x B + bias).
+ *   A     [M, K] ab_dtype (F16 or BF16), row-major
+ *   B     [K, N] ab_dtype, row-major (N contiguous; not transposed)
+ *   bias  [N] fp32, or NULL
+ *   C     [M, N] c_dtype (F32, F16 or BF16), row-major; fully overwritten
+ *   alpha LeakyReLU slope (ignored by the other activations)
+ * Accumulation is fp32 on the tensor cores.  M == 0 or N == 0 enqueues
+ * nothing; K == 0 gives C = act(bias).  Requires K % 8 == 0 and N % 8 == 0
+ * (16-byte row pitch) else MMACT_ERR_UNSUPPORTED; M, N, K < 2^31.
+ */
+mmact_status mmact_gemm(const void *A, const void *B, const float *bias, void *C,
+                        int64_t M, int64_t N, int64_t K,
+                        mmact_dtype ab_dtype, mmact_dtype c_dtype,
+                        mmact_act act, float alpha, void *stream);
+
+/*
+ * Two-kernel ablation of mmact_gemm.  Kernel 1 writes z = A x B + bias in fp32
+ * to `workspace` ([M, N] fp32, caller-allocated, M*N*4 bytes, 16-byte
+ * aligned); kernel 2 reads it, applies act in fp32 and writes C.  Same result
+ * contract as mmact_gemm; the workspace holds z afterwards.
+ */
+mmact_status mmact_gemm_split(const void *A, const void *B, const float *bias, void *C,
+                              int64_t M, int64_t N, int64_t K,
+                              mmact_dtype ab_dtype, mmact_dtype c_dtype,
+                              mmact_act act, float alpha, float *workspace, void *stream);
+
+/*
+ * Fused implicit-GEMM conv2d + bias + activation:  y = act(conv2d(x, w) + bias).
+ *   x    [N, C, H, W] in_dtype (F16 or BF16), NCHW
+ *   w    [Co, C, kh, kw] in_dtype
+ *   bias [Co] fp32, or NULL
+ *   y    [N, Co, Ho, Wo] out_dtype (F32, F16 or BF16), NCHW; fully overwritten
+ *   strides   = {sh, sw} >= 1
+ *   pads      = {top, bottom, left, right} >= 0 (zero padding)
+ *   dilations = {dh, dw} >= 1
+ *   Ho = floor((H + top + bottom - dh*(kh-1) - 1) / sh) + 1, Wo likewise;
+ *   a geometry with Ho < 1 or Wo < 1 is MMACT_ERR_INVALID_ARG.
+ * N == 0 or Co == 0 enqueues nothing; C == 0 gives y = act(bias).
+ */
+mmact_status mmact_conv2d(const void *x, const void *w, const float *bias, void *y,
+                          int64_t N, int64_t C, int64_t H, int64_t W,
+                          int64_t Co, int64_t kh, int64_t kw,
+                          const int32_t strides[2], const int32_t pads[4],
+                          const int32_t dilations[2],
+                          mmact_dtype in_dtype, mmact_dtype out_dtype,
+                          mmact_act act, float alpha, void *stream);
+
+/*
+ * Two-kernel ablation of mmact_conv2d: kernel 1 writes z (conv + bias, fp32)
+ * to `workspace` ([N, Co, Ho, Wo] fp32, caller-allocated, 16-byte aligned),
+ * kernel 2 applies act and writes y.
+ */
+mmact_status mmact_conv2d_split(const void *x, const void *w, const float *bias, void *y,
+                                int64_t N, int64_t C, int64_t H, int64_t W,
+                                int64_t Co, int64_t kh, int64_t kw,
+                                const int32_t strides[2], const int32_t pads[4],
+                                const int32_t dilations[2],
+                                mmact_dtype in_dtype, mmact_dtype out_dtype,
+                                mmact_act act, float alpha, float *workspace, void *stream);
+
+/*
+ * Output spatial size of a conv geometry (host only, no CUDA call).  Writes
+ * Ho and Wo (host pointers) and returns MMACT_OK, or MMACT_ERR_INVALID_ARG for
+ * a bad geometry (non-positive kernel/stride/dilation, negative pad or size,
+ * or an empty output).
+ */
+mmact_status mmact_conv2d_out_shape(int64_t H, int64_t W, int64_t kh, int64_t kw,
+                                    const int32_t strides[2], const int32_t pads[4],
+                                    const int32_t dilations[2], int64_t *Ho, int64_t *Wo);
+
+/*
+ * Synchronises `stream`, then reports and clears the current device's kernel
+ * status word: MMACT_OK, MMACT_ERR_TIMEOUT (a bounded wait inside a kernel ran
+ * out; the kernel skipped its remaining work and left its outputs
+ * unspecified), or MMACT_ERR_CUDA (the stream reported a CUDA error).
+ */
+mmact_status mmact_get_last_error(void *stream);
+
+/*
+ * Upper bound, in nanoseconds, on every wait inside the pipelined kernels
+ * (default 2e9).  A wait that runs out makes the kernel stop, release its
+ * tensor memory and record MMACT_ERR_TIMEOUT.  Applies to launches made after
+ * the call.  0 restores the default.
+ */
+void mmact_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Diagnostic: enqueue one tiny kernel on `stream` that waits on an mbarrier
+ * nothing ever arrives at, bounded by `timeout_ns`; it records
+ * MMACT_ERR_TIMEOUT in the status word and returns.  Used to check the
+ * timeout-reporting path without any fault.
+ */
+mmact_status mmact_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+/*
+ * Tuning and testing aid: force the N-extent of the GEMM output tile (64, 128
+ * or 256; 0 = automatic choice).  Applies to later mmact_gemm* calls in the
+ * process.  Returns MMACT_ERR_INVALID_ARG for other values.
+ */
+mmact_status mmact_set_gemm_tile_n(int tile_n);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *mmact_status_string(mmact_status status);
+
+/* ABI version of this header: 1. */
+int mmact_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MMACT_H */

@@ -1,0 +1,139 @@
+"""The C ABI library loads and exports every symbol include/mmact.h declares,
+and its host-only paths (argument validation, output shape) behave.  No GPU
+is needed: every call here returns before any CUDA work."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from conv_activation_epilogue_gb300 import build, mmact
+import oracle
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mmact.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mmact_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return mmact.load()
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(mmact.SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIBRARY], capture_output=True,
+                         text=True, check=True).stdout
+    exported = sorted(set(re.findall(r"\b(mmact_[a-z0-9_]+)$", out, flags=re.M)))
+    assert exported == declared_functions()
+
+
+def test_version_and_status_strings(lib):
+    assert mmact.mmact_version() == 1
+    for s in range(5):
+        assert mmact.mmact_status_string(s).startswith("MMACT_")
+    assert "unknown" in mmact.mmact_status_string(99)
+
+
+def test_tile_override_validation(lib):
+    for bad in (1, 32, 96, 512, -64):
+        assert lib.mmact_set_gemm_tile_n(bad) == mmact.MMACT_ERR_INVALID_ARG
+    for good in (64, 128, 256, 0):
+        assert lib.mmact_set_gemm_tile_n(good) == mmact.MMACT_OK
+
+
+def test_out_shape_matches_oracle(lib):
+    orc = oracle.get()
+    for (H, W, kh, kw, st, pd, dl) in [(56, 56, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1)),
+                                       (64, 64, 3, 3, (2, 2), (2, 2, 2, 2), (2, 2)),
+                                       (64, 64, 1, 1, (2, 2), (0, 0, 0, 0), (1, 1)),
+                                       (7, 5, 3, 2, (2, 1), (1, 0, 2, 1), (1, 2)),
+                                       (1, 1, 1, 1, (3, 3), (0, 0, 0, 0), (1, 1))]:
+        Ho, Wo = mmact.mmact_conv2d_out_shape(H, W, kh, kw, st, pd, dl)
+        assert Ho == orc.conv_out_dim(H, kh, st[0], pd[0], pd[1], dl[0])
+        assert Wo == orc.conv_out_dim(W, kw, st[1], pd[2], pd[3], dl[1])
+
+
+def test_out_shape_rejects_bad_geometry(lib):
+    for args in [(5, 5, 0, 3, (1, 1), (0, 0, 0, 0), (1, 1)),
+                 (5, 5, 3, 3, (0, 1), (0, 0, 0, 0), (1, 1)),
+                 (5, 5, 3, 3, (1, 1), (-1, 0, 0, 0), (1, 1)),
+                 (5, 5, 3, 3, (1, 1), (0, 0, 0, 0), (0, 1)),
+                 (2, 2, 3, 3, (1, 1), (0, 0, 0, 0), (1, 1))]:   # empty output
+        with pytest.raises(mmact.MmactError) as ei:
+            mmact.mmact_conv2d_out_shape(*args)
+        assert ei.value.status == mmact.MMACT_ERR_INVALID_ARG
+
+
+# Fake, never-dereferenced device addresses: every call below is rejected on
+# the host before any CUDA call, or is a no-op (empty problem).
+P16 = 0x7f0000000000
+P_MIS = P16 + 2
+
+
+def gemm(lib, A=P16, B=P16, bias=None, C=P16, M=64, N=64, K=64, ab=1, cd=1, act=2, ws=None,
+         split=False):
+    if split:
+        return lib.mmact_gemm_split(A, B, bias, C, M, N, K, ab, cd, act, ctypes.c_float(0.1), ws, None)
+    return lib.mmact_gemm(A, B, bias, C, M, N, K, ab, cd, act, ctypes.c_float(0.1), None)
+
+
+def test_gemm_host_validation(lib):
+    E, U, OK = mmact.MMACT_ERR_INVALID_ARG, mmact.MMACT_ERR_UNSUPPORTED, mmact.MMACT_OK
+    assert gemm(lib, A=None) == E
+    assert gemm(lib, B=None) == E
+    assert gemm(lib, C=None) == E
+    assert gemm(lib, M=-1) == E
+    assert gemm(lib, K=-8) == E
+    assert gemm(lib, N=1 << 31) == E
+    assert gemm(lib, ab=2) == E             # fp32 operands are not a kind::f16 input
+    assert gemm(lib, ab=7) == E
+    assert gemm(lib, cd=5) == E
+    assert gemm(lib, act=4) == E
+    assert gemm(lib, act=-1) == E
+    assert gemm(lib, bias=P16 + 1) == E     # bias must be 4-byte aligned
+    assert gemm(lib, A=P_MIS) == U
+    assert gemm(lib, C=P_MIS) == U
+    assert gemm(lib, K=60) == U             # row pitch of A not a multiple of 16 bytes
+    assert gemm(lib, N=60) == U
+    assert gemm(lib, M=0) == OK             # empty: nothing enqueued
+    assert gemm(lib, N=0) == OK
+    assert gemm(lib, split=True, ws=None) == E
+    assert gemm(lib, split=True, ws=P_MIS) == U
+    assert gemm(lib, split=True, ws=P16, M=0) == OK
+
+
+def test_conv_host_validation(lib):
+    E, U = mmact.MMACT_ERR_INVALID_ARG, mmact.MMACT_ERR_UNSUPPORTED
+    i32 = lambda *v: (ctypes.c_int32 * len(v))(*v)  # noqa: E731
+
+    def conv(x=P16, w=P16, y=P16, N=1, C=4, H=8, W=8, Co=4, kh=3, kw=3, st=(1, 1),
+             pd=(1, 1, 1, 1), dl=(1, 1), i=1, o=1, act=3):
+        return lib.mmact_conv2d(x, w, None, y, N, C, H, W, Co, kh, kw, i32(*st), i32(*pd), i32(*dl),
+                                i, o, act, ctypes.c_float(0), None)
+
+    assert conv(x=None) == E
+    assert conv(y=None) == E
+    assert conv(N=-1) == E
+    assert conv(kh=0) == E
+    assert conv(st=(0, 1)) == E
+    assert conv(pd=(0, -1, 0, 0)) == E
+    assert conv(dl=(1, 0)) == E
+    assert conv(H=1, pd=(0, 0, 0, 0)) == E   # 3x3 filter on a 1-row input: empty output
+    assert conv(i=2) == E
+    assert conv(o=3) == E
+    assert conv(act=9) == E
+    assert conv(x=P_MIS) == U
+    assert lib.mmact_conv2d(P16, P16, None, P16, 1, 4, 8, 8, 4, 3, 3, None, i32(0, 0, 0, 0),
+                            i32(1, 1), 1, 1, 3, ctypes.c_float(0), None) == E
