@@ -170,8 +170,10 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
 mmact_status gemm_check(const void *A, const void *B, const float *bias, const void *C, int64_t M,
                         int64_t N, int64_t K, mmact_dtype ab, mmact_dtype cd, mmact_act act)
 {
-    if (A == nullptr || B == nullptr || C == nullptr) return MMACT_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0 || M > MAX_DIM || N > MAX_DIM || K > MAX_DIM)
+        return MMACT_ERR_INVALID_ARG;
+    // a pointer may be null only when its tensor is empty
+    if ((A == nullptr && M * K != 0) || (B == nullptr && K * N != 0) || (C == nullptr && M * N != 0))
         return MMACT_ERR_INVALID_ARG;
     if (!valid_in(ab) || !valid_out(cd) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
     if (bias != nullptr && !aligned4(bias)) return MMACT_ERR_INVALID_ARG;
@@ -204,11 +206,14 @@ mmact_status conv_check(const void *x, const void *w, const float *bias, const v
                         const int32_t *st, const int32_t *pd, const int32_t *dl, mmact_dtype in,
                         mmact_dtype out, mmact_act act, ConvGeom *g)
 {
-    if (x == nullptr || w == nullptr || y == nullptr) return MMACT_ERR_INVALID_ARG;
     if (N < 0 || C < 0 || Co < 0) return MMACT_ERR_INVALID_ARG;
     if (!valid_in(in) || !valid_out(out) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
     mmact_status s = conv_geom(H, W, kh, kw, st, pd, dl, g);
     if (s != MMACT_OK) return s;
+    // a pointer may be null only when its tensor is empty
+    if ((x == nullptr && N * C * H * W != 0) || (w == nullptr && Co * C != 0) ||
+        (y == nullptr && N * Co != 0))
+        return MMACT_ERR_INVALID_ARG;
     if (bias != nullptr && !aligned4(bias)) return MMACT_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return MMACT_ERR_UNSUPPORTED;
     // every index the kernel forms fits in 32 bits per image / 64 bits overall

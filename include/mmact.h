@@ -33,7 +33,8 @@
  *     never allocates, frees or retains them.
  *   - All tensors are dense and row-major (C order).  16-byte alignment is
  *     required of A, B, C, x, y, w and workspace; 4-byte alignment of bias.
- *   - bias may be NULL (treated as all zeros).
+ *   - bias may be NULL (treated as all zeros).  Any other pointer may be NULL
+ *     only when its tensor has no elements.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are asynchronous: they validate arguments on the host,
  *     enqueue kernels on `stream` and return.  A status other than MMACT_OK

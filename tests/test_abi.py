@@ -107,6 +107,7 @@ def test_gemm_host_validation(lib):
     assert gemm(lib, C=P_MIS) == U
     assert gemm(lib, K=60) == U             # row pitch of A not a multiple of 16 bytes
     assert gemm(lib, N=60) == U
+    assert gemm(lib, A=None, M=0) == OK     # an empty tensor may have a null pointer
     assert gemm(lib, M=0) == OK             # empty: nothing enqueued
     assert gemm(lib, N=0) == OK
     assert gemm(lib, split=True, ws=None) == E
