@@ -25,7 +25,7 @@ _lib = None
 
 # Exported C symbols, as declared in include/mmact.h.
 SYMBOLS = [
-    "mmact_gemm", "mmact_gemm_split", "mmact_conv2d", "mmact_conv2d_split",
+    "mmact_gemm", "mmact_gemm_split", "mmact_gemm_split_noalloc", "mmact_conv2d", "mmact_conv2d_split",
     "mmact_conv2d_out_shape", "mmact_get_last_error", "mmact_set_wait_timeout_ns",
     "mmact_selftest_wait_timeout", "mmact_set_gemm_tile_n", "mmact_status_string", "mmact_version",
 ]
@@ -52,6 +52,8 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     p_i32 = ctypes.POINTER(i32)
     L.mmact_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, f32, vp]
     L.mmact_gemm_split.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, f32, vp, vp]
+    L.mmact_gemm_split_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, f32, vp]
+    L.mmact_gemm_split_noalloc.restype = ci
     conv = [vp, vp, vp, vp] + [i64] * 7 + [p_i32, p_i32, p_i32, ci, ci, ci, f32]
     L.mmact_conv2d.argtypes = conv + [vp]
     L.mmact_conv2d_split.argtypes = conv + [vp, vp]
@@ -144,6 +146,20 @@ def mmact_gemm_split(A, B, bias, C, workspace, act: str = "none", alpha: float =
         raise ValueError("workspace must hold M*N fp32 elements")
     _check(L.mmact_gemm_split(pa, pb, pbias, pc, M, N, K, DTYPE[A.dtype], DTYPE[C.dtype], ACT[act],
                               float(alpha), pw, _stream_handle(stream)), "mmact_gemm_split")
+
+
+NOALLOC_MAX_ELEMENTS = 4194304   # MMACT_NOALLOC_MAX_ELEMENTS in include/mmact.h
+
+
+def mmact_gemm_split_noalloc(A, B, bias, C, act: str = "none", alpha: float = 0.0,
+                             stream=None) -> None:
+    """mmact_gemm_split using the library's built-in scratch array instead of a
+    caller-provided workspace (for callers that cannot allocate; M*N is limited)."""
+    L = load()
+    pa, pb, pbias, pc, M, N, K = _gemm_args(A, B, bias, C)
+    _check(L.mmact_gemm_split_noalloc(pa, pb, pbias, pc, M, N, K, DTYPE[A.dtype], DTYPE[C.dtype],
+                                      ACT[act], float(alpha), _stream_handle(stream)),
+           "mmact_gemm_split_noalloc")
 
 
 def _i32(vals, n):

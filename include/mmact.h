@@ -137,6 +137,42 @@ mmact_status mmact_conv2d_split(const void *x, const void *w, const float *bias,
                                 mmact_act act, float alpha, float *workspace, void *stream);
 
 /*
+ * Largest M*N accepted by mmact_gemm_split_noalloc (fp32 elements of its
+ * built-in scratch array: 16 MiB per device).
+ */
+#define MMACT_NOALLOC_MAX_ELEMENTS 4194304
+
+/*
+ * mmact_gemm_split for callers that cannot allocate device memory when they
+ * call the library.  (The pages have no counterpart: this entry point exists
+ * for deployment, not for the method.)  Some callers are only handed their
+ * input and output buffers by a host framework, run under a framework
+ * allocator that already owns the device budget, or sit in a latency-critical
+ * loop where cudaMalloc / cudaFree could block or synchronise the device;
+ * they cannot supply the M*N fp32 workspace the split path needs.  This entry
+ * point takes the same arguments as mmact_gemm_split minus `workspace`, and
+ * uses a fixed scratch array compiled into the library instead; it calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   - Limit: M*N <= MMACT_NOALLOC_MAX_ELEMENTS, else MMACT_ERR_UNSUPPORTED
+ *     (nothing enqueued).  Every GPU that loads the library holds the 16 MiB
+ *     array until the process exits.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress, with that device current) and caches it;
+ *     make that first call before any stream capture.
+ *   - Sharing: all calls on a device share the one array, which keeps the
+ *     last call's intermediate values.  Nothing in it needs clearing: the
+ *     first kernel overwrites every element it uses before the second reads
+ *     it.  Calls whose kernels may overlap on the GPU (different streams, or
+ *     several host threads without ordering) race on the array; order them,
+ *     e.g. on one stream.
+ * All other behaviour, layouts and errors are those of mmact_gemm_split.
+ */
+mmact_status mmact_gemm_split_noalloc(const void *A, const void *B, const float *bias, void *C,
+                                      int64_t M, int64_t N, int64_t K,
+                                      mmact_dtype ab_dtype, mmact_dtype c_dtype,
+                                      mmact_act act, float alpha, void *stream);
+
+/*
  * Output spatial size of a conv geometry (host only, no CUDA call).  Writes
  * Ho and Wo (host pointers) and returns MMACT_OK, or MMACT_ERR_INVALID_ARG for
  * a bad geometry (non-positive kernel/stride/dilation, negative pad or size,
