@@ -55,7 +55,8 @@ mmact_status device_info(DeviceInfo **out)
             return MMACT_ERR_CUDA;
         if (cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_status) != cudaSuccess)
             return MMACT_ERR_CUDA;
-        if (setup_gemm_kernels() != cudaSuccess || setup_conv_kernels() != cudaSuccess)
+        if (setup_gemm_kernels() != cudaSuccess || setup_conv_kernels() != cudaSuccess ||
+            setup_conv_vec_kernels() != cudaSuccess)
             return MMACT_ERR_CUDA;
         if (g_encode == nullptr) {
             void *fn = nullptr;
@@ -274,8 +275,37 @@ mmact_status conv_enqueue(const void *x, const void *w, const float *bias, void 
     a.wait_ns = g_wait_ns.load();
     a.a_tma = (a.K % 8 == 0) ? 1 : 0;
     a.y_tma = ((P * a.out_elem_bytes) % 16 == 0) ? 1 : 0;
+    // Vectorised producer: whole 16-byte input chunks per row (W % 8 == 0),
+    // horizontal stride 1 or 2, filter by TMA, and an output TMA store:
+    // 8 x 32 tiles when the output is exactly 32 wide (256 consecutive
+    // pixels), else 4 x 64 tiles stored through a 4-D map (rows of y must be
+    // 16-byte multiples).
+    a.W8 = (int)(W / 8);
+    if (a.a_tma && W % 8 == 0 && (a.sw == 1 || a.sw == 2)) {
+        if (g.Wo == 32 && a.y_tma) {
+            a.vec = 1;
+            a.TW = 32;
+            a.TH = 8;
+        } else if ((g.Wo * a.out_elem_bytes) % 16 == 0) {
+            a.vec = 1;
+            a.TW = 64;
+            a.TH = 4;
+        }
+    }
+    if (a.vec) {
+        a.tiles_oh = (int)((g.Ho + a.TH - 1) / a.TH);
+        a.tiles_ow = (int)((g.Wo + a.TW - 1) / a.TW);
+        a.num_tiles = (int)(N * a.tiles_oh * a.tiles_ow * a.tiles_co);
+    }
     L.out = out_kind(out);
     L.grid = (int)std::min<int64_t>(a.num_tiles, dev->sm_count);
+    if (a.vec && a.TW == 64) {
+        const int e = a.out_elem_bytes;
+        const uint64_t d[4] = {(uint64_t)g.Wo, (uint64_t)g.Ho, (uint64_t)Co, (uint64_t)N};
+        const uint64_t sb[3] = {(uint64_t)g.Wo * e, (uint64_t)P * e, (uint64_t)Co * P * e};
+        const uint32_t bx[4] = {(uint32_t)(128 / e), 1, 32, 1};
+        if (!encode(&L.tmY4, out, 4, y, d, sb, bx)) return MMACT_ERR_CUDA;
+    }
     if (a.a_tma) {
         const uint64_t d[2] = {(uint64_t)a.K, (uint64_t)Co}, sb[1] = {(uint64_t)a.K * 2};
         const uint32_t bx[2] = {64, 128};

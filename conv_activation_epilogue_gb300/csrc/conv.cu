@@ -152,8 +152,13 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
                                  ptx::idesc_f16(p.ab_bf16 != 0, false, true, 128, BN));
     } else if (warp >= 6) {
         // ---------------------------------------------------- B-tile gather --
+        // Thread j owns pixel column j of every B tile.  For each stage it
+        // first issues all 64 of its loads into registers -- independent, so
+        // they are in flight together, and issued before waiting for the ring
+        // slot so their latency overlaps the wait -- then writes them into
+        // the swizzled tile.
         const int j = threadIdx.x - 192;              // this thread's pixel column, 0..127
-        const int64_t HW = (int64_t)p.H * p.W;
+        const int HW = p.H * p.W;                     // C*H*W < 2^31 is checked on the host
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
@@ -167,28 +172,28 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
             const uint16_t *xn = p.x + (int64_t)n * p.C * HW;
             const int co_rows = p.Co - cb * 128;      // filter rows valid in this tile (gathered A)
             // (ci, r, q) of the next K index, advanced one step per element
-            int ci = 0, r = 0, q = 0, k = 0;
+            int r = 0, q = 0, k = 0, cbase = 0;       // cbase = ci * H * W
             for (int kb = 0; kb < p.num_kb; ++kb) {
+                uint16_t vals[64];
+#pragma unroll
+                for (int kl = 0; kl < 64; ++kl) {
+                    const int ih = ih0 + r * p.dh, iw = iw0 + q * p.dw;
+                    const bool in = pvalid && k < p.K && (unsigned)ih < (unsigned)p.H &&
+                                    (unsigned)iw < (unsigned)p.W;
+                    vals[kl] = in ? __ldg(xn + cbase + ih * p.W + iw) : (uint16_t)0;
+                    ++k;
+                    if (++q == p.kw) {
+                        q = 0;
+                        if (++r == p.kh) { r = 0; cbase += HW; }
+                    }
+                }
                 uint32_t go = 1;
                 if (lane == 0) go = pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u) ? 1u : 0u;
                 go = __shfl_sync(0xffffffffu, go, 0);
                 if (!go) { ok = false; break; }
                 const uint32_t bt = sB + stage * Cfg::B_BYTES;
-#pragma unroll 4
-                for (int kl = 0; kl < 64; ++kl) {
-                    uint16_t v = 0;
-                    if (k < p.K) {
-                        const int ih = ih0 + r * p.dh, iw = iw0 + q * p.dw;
-                        if (pvalid && (unsigned)ih < (unsigned)p.H && (unsigned)iw < (unsigned)p.W)
-                            v = __ldg(xn + (int64_t)ci * HW + (int64_t)ih * p.W + iw);
-                    }
-                    ptx::st_shared_u16(bt + b_tile_offset(kl, j), v);
-                    ++k;
-                    if (++q == p.kw) {
-                        q = 0;
-                        if (++r == p.kh) { r = 0; ++ci; }
-                    }
-                }
+#pragma unroll
+                for (int kl = 0; kl < 64; ++kl) ptx::st_shared_u16(bt + b_tile_offset(kl, j), vals[kl]);
                 if (!p.a_tma) {
                     // filter tile rows m = j: w[cb*128 + m][kb*64 .. +64)
                     const uint32_t at = sA + stage * Cfg::A_BYTES;
@@ -303,6 +308,7 @@ cudaError_t setup_conv_kernels()
 
 cudaError_t launch_conv(const ConvLaunch &L, cudaStream_t stream)
 {
+    if (L.args.vec) return launch_conv_vec(L, stream);
     if (L.out == OUT_BF16) return launch_conv_t<OUT_BF16>(L, stream);
     if (L.out == OUT_F16) return launch_conv_t<OUT_F16>(L, stream);
     if (L.out == OUT_F32) return launch_conv_t<OUT_F32>(L, stream);

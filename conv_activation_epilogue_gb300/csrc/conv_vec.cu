@@ -1,0 +1,368 @@
+// conv_vec.cu -- implicit-GEMM conv2d + bias + activation, vectorised
+// producer for the common NCHW geometries (input width a multiple of 8,
+// horizontal stride 1 or 2, filter rows whose pitch allows TMA).
+//
+// Same GEMM view as conv.cu ("multimodal-ops Fused ConvTanh" article, section
+// on how the two kernels split the work: A = filter [Co x Ci*kh*kw], B = input
+// features [Ci*kh*kw x pixels], result [Co, pixels] = NCHW), with a 128 x 256
+// output tile: 128 output channels x 256 output pixels, the pixels being TH
+// output rows x TW output columns (4 x 64, or 8 x 32 when the output is exactly
+// 32 wide, in which case the tile is 256 consecutive pixels of one image).
+//
+// B-tile producer.  Each gather warp owns 16 consecutive K rows (ci, r, q) of
+// every 64-row stage; for each row every lane builds one 16-byte vector of 8
+// consecutive output pixels.  Those pixels read input row
+// ih = oh*sh - pt + r*dh at columns iws + S*e (e = 0..7), iws = ow*S - pl + q*dw.
+// Because W is a multiple of 8, the input row splits into aligned 8-element
+// chunks that never straddle two rows; the lane loads the 2 (S = 1) or 3
+// (S = 2) aligned chunks covering the window -- chunks outside the row or rows
+// outside the image read as zero, which is exactly the zero padding -- and
+// picks its 8 elements with byte permutes.  The shift iws mod 8 is the same
+// for every lane of the warp, so the selection is a warp-uniform switch.  The
+// vector is stored with one 16-byte shared store into the 128-byte swizzled
+// MN-major tile that tcgen05.mma reads.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mmact {
+
+struct ConvVecCfg {
+    static constexpr int BM = 128, BN = 256, BK = 64;
+    static constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+    static constexpr int B_BYTES = BK * BN * 2;          // 32 KB (4 chunks of 64 pixels)
+    static constexpr int STAGES = 4;
+    static constexpr int EPI_BYTES = 4 * 2 * 4096;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16;
+    static constexpr int GATHER_WARPS = 8;
+    static constexpr int THREADS = (6 + GATHER_WARPS) * 32;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// tile -> (image, output-row block, output-column block, channel block); the
+// channel block varies fastest so neighbouring CTAs share input pixels in L2.
+__device__ __forceinline__ void vconv_tile(int t, const ConvArgs &p, int &n, int &toh, int &tow,
+                                           int &cb)
+{
+    cb = t % p.tiles_co;
+    int r = t / p.tiles_co;
+    tow = r % p.tiles_ow;
+    r /= p.tiles_ow;
+    toh = r % p.tiles_oh;
+    n = r / p.tiles_oh;
+}
+
+__device__ __forceinline__ uint4 ldg16(const uint16_t *p)
+{
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// Eight output elements e = 0..7 taken from the concatenated chunk words w at
+// element positions SH + S*e.
+template <int S, int SH>
+__device__ __forceinline__ void pick8(const uint32_t *w, uint32_t (&o)[4])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if constexpr (S == 1) {
+            const int a = SH / 2 + j;
+            o[j] = (SH & 1) ? __byte_perm(w[a], w[a + 1], 0x5432) : w[a];
+        } else {
+            const int a = SH / 2 + 2 * j;
+            o[j] = (SH & 1) ? __byte_perm(w[a], w[a + 1], 0x7632) : __byte_perm(w[a], w[a + 1], 0x5410);
+        }
+    }
+}
+
+template <int S>
+__device__ __forceinline__ void pick8_dispatch(int sh, const uint32_t *w, uint32_t (&o)[4])
+{
+    switch (sh) {
+    case 0: pick8<S, 0>(w, o); break;
+    case 1: pick8<S, 1>(w, o); break;
+    case 2: pick8<S, 2>(w, o); break;
+    case 3: pick8<S, 3>(w, o); break;
+    case 4: pick8<S, 4>(w, o); break;
+    case 5: pick8<S, 5>(w, o); break;
+    case 6: pick8<S, 6>(w, o); break;
+    default: pick8<S, 7>(w, o); break;
+    }
+}
+
+template <int OUT, int S>
+__global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
+    conv_vec_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmY,
+                    const __grid_constant__ CUtensorMap tmY4, const ConvArgs p)
+{
+    using Cfg = ConvVecCfg;
+    constexpr int STAGES = Cfg::STAGES, BN = Cfg::BN;
+    constexpr int COLS = OUT == OUT_F32 ? 32 : 64;
+    constexpr int NCH = S == 1 ? 2 : 3;                 // aligned chunks per output vector
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const uint32_t base = ptx::smem_addr(smem);
+    if (base & 1023u) {
+        if (threadIdx.x == 0) atomicOr(p.status, ST_SMEM_ALIGN);
+        return;
+    }
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
+    Pipe pp;
+    pp.full0 = base + Cfg::OFF_BAR;
+    pp.empty0 = pp.full0 + 8 * STAGES;
+    pp.tfull0 = pp.empty0 + 8 * STAGES;
+    pp.tempty0 = pp.tfull0 + 16;
+    pp.drain = pp.tempty0 + 16;
+    pp.abort = misc + 1;
+    pp.status = p.status;
+    pp.wait_ns = p.wait_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(pp.full0 + 8 * s, Cfg::GATHER_WARPS + 1);   // gather warps + filter TMA
+            ptx::mbar_init(pp.empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(pp.tfull0 + 8 * a, 1);
+            ptx::mbar_init(pp.tempty0 + 8 * a, 4);
+        }
+        ptx::mbar_init(pp.drain, 1);
+        misc[1] = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(base + Cfg::OFF_MISC, Cfg::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    pp.tmem = misc[0];
+
+    const uint32_t sA = base + Cfg::OFF_A, sB = base + Cfg::OFF_B;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------- filter producer --
+            ptx::prefetch_tensormap(&tmW);
+            uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+                int n, toh, tow, cb;
+                vconv_tile(t, p, n, toh, tow, cb);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u)) { ok = false; break; }
+                    const uint32_t fb = pp.full0 + 8 * stage;
+                    ptx::mbar_arrive_expect_tx(fb, Cfg::A_BYTES);
+                    ptx::tma_load_2d(sA + stage * Cfg::A_BYTES, &tmW, fb, kb * 64, cb * 128);
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) pipe_fail(pp);
+            for (int s = 0; s < STAGES; ++s)
+                if (issued & (1u << s))
+                    ptx::mbar_wait_bounded(pp.full0 + 8 * s, (last_par >> s) & 1u, DRAIN_NS, nullptr);
+        }
+    } else if (warp == 1) {
+        if (lane == 0)
+            mma_role<BN, STAGES>(pp, sA, sB, p.num_tiles, p.num_kb,
+                                 ptx::idesc_f16(p.ab_bf16 != 0, false, true, 128, BN));
+    } else if (warp >= 6) {
+        // ---------------------------------------------------- B-tile gather --
+        // Rows are handled in groups of 4: the loads of a whole group are
+        // issued before any of its byte-picks, and the first group's loads go
+        // out before the wait for the ring slot, so load latency overlaps.
+        constexpr int ROWS = 64 / Cfg::GATHER_WARPS;     // K rows per warp and stage
+        constexpr int GRP = 4;
+        const int gw = warp - 6;                         // owns K rows [gw*ROWS, +ROWS) of a stage
+        const int HW = p.H * p.W;
+        const int taps = p.kh * p.kw;
+        const int vpr = p.TW >> 3;                       // vectors per tile row: 8 or 4
+        const int t_row = lane / vpr, t_vec = lane - (lane / vpr) * vpr;
+        const int pcol = t_row * p.TW + t_vec * 8;       // B-tile column of this lane's first pixel
+        const uint32_t lane_off = (uint32_t)((pcol >> 6) * 8192);
+        const uint32_t pc8 = (uint32_t)((pcol >> 3) & 7);
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+            int n, toh, tow, cb;
+            vconv_tile(t, p, n, toh, tow, cb);
+            const int oh = toh * p.TH + t_row;
+            const int ihb = oh * p.sh - p.pt;
+            const int iwb = (tow * p.TW + t_vec * 8) * S - p.pl;
+            const uint16_t *xn = p.x + (int64_t)n * p.C * HW;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                int k = kb * 64 + gw * ROWS;
+                int ci = k / taps;
+                int rem = k - ci * taps;
+                int r = rem / p.kw;
+                int q = rem - r * p.kw;
+                const uint32_t bt = sB + stage * Cfg::B_BYTES + lane_off;
+#pragma unroll 1
+                for (int g = 0; g < ROWS; g += GRP) {
+                    uint4 ch[GRP][NCH];
+                    int shift[GRP];
+#pragma unroll
+                    for (int i = 0; i < GRP; ++i) {
+                        const int ih = ihb + r * p.dh;
+                        const int iws = iwb + q * p.dw;
+                        const int c0 = iws >> 3;                 // floor(iws / 8)
+                        const bool rowok = k < p.K && (unsigned)ih < (unsigned)p.H;
+                        const uint16_t *rowp = xn + ci * HW + ih * p.W;
+                        shift[i] = iws & 7;
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) {
+                            ch[i][c] = make_uint4(0u, 0u, 0u, 0u);
+                            if (rowok && (unsigned)(c0 + c) < (unsigned)p.W8) ch[i][c] = ldg16(rowp + (c0 + c) * 8);
+                        }
+                        ++k;
+                        if (++q == p.kw) {
+                            q = 0;
+                            if (++r == p.kh) { r = 0; ++ci; }
+                        }
+                    }
+                    if (g == 0) {
+                        uint32_t go = 1;
+                        if (lane == 0) go = pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u) ? 1u : 0u;
+                        go = __shfl_sync(0xffffffffu, go, 0);
+                        if (!go) { ok = false; break; }
+                    }
+#pragma unroll
+                    for (int i = 0; i < GRP; ++i) {
+                        uint32_t w[4 * NCH];
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) {
+                            w[4 * c + 0] = ch[i][c].x;
+                            w[4 * c + 1] = ch[i][c].y;
+                            w[4 * c + 2] = ch[i][c].z;
+                            w[4 * c + 3] = ch[i][c].w;
+                        }
+                        uint32_t o[4];
+                        pick8_dispatch<S>(shift[i], w, o);
+                        const int kl = gw * ROWS + g + i;
+                        ptx::st_shared_v4(bt + (uint32_t)kl * 128u + ((pc8 ^ (uint32_t)(kl & 7)) << 4), o[0],
+                                          o[1], o[2], o[3]);
+                    }
+                }
+                if (!ok) break;
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(pp.full0 + 8 * stage);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!ok) pipe_fail(pp);
+    } else {
+        // -------------------------------------------------------- epilogue --
+        const int qd = warp & 3;
+        const uint32_t my_buf = base + Cfg::OFF_EPI + (uint32_t)qd * 8192u;
+        uint32_t acc = 0, acc_phase = 0, units = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+            int n, toh, tow, cb;
+            vconv_tile(t, p, n, toh, tow, cb);
+            const int co_row0 = cb * 128 + qd * 32;
+            const int co = co_row0 + lane;
+            const float brow = (p.bias != nullptr && co < p.Co) ? __ldg(p.bias + co) : 0.0f;
+            uint32_t got = 1;
+            if (lane == 0) got = pipe_wait(pp, pp.tfull0 + 8 * acc, acc_phase) ? 1u : 0u;
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t tbase = pp.tmem + ((uint32_t)(qd * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int u = 0; u < BN / COLS; ++u) {
+                const uint32_t buf = my_buf + (units++ & 1u) * 4096u;
+                if (lane == 0) ptx::bulk_wait_read<1>();
+                __syncwarp();
+                epi_unit_dispatch<OUT, true>(p.act, tbase + u * COLS, nullptr, 0, brow, p.alpha, buf, lane);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && co_row0 < p.Co) {
+                    const int col = u * COLS;                // first B-tile column of this unit
+                    if (p.TW == 32) {
+                        // the tile is 256 consecutive pixels of image n
+                        const int pix0 = toh * p.TH * p.Wo + col;
+                        if (pix0 < p.P) {
+                            ptx::tma_store_3d(&tmY, buf, pix0, co_row0, n);
+                            ptx::bulk_commit();
+                        }
+                    } else {
+                        const int oh = toh * p.TH + col / 64;
+                        const int ow = tow * 64 + (col & 63);
+                        if (oh < p.Ho && ow < p.Wo) {
+                            ptx::tma_store_4d(&tmY4, buf, ow, oh, co_row0, n);
+                            ptx::bulk_commit();
+                        }
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(pp.tempty0 + 8 * acc);
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (!ok) pipe_fail(pp);
+        if (lane == 0) ptx::bulk_wait<0>();
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(pp.tmem, Cfg::TMEM_COLS);
+    }
+}
+
+template <int OUT, int S>
+static cudaError_t launch_vec_t(const ConvLaunch &L, cudaStream_t stream)
+{
+    conv_vec_kernel<OUT, S><<<L.grid, ConvVecCfg::THREADS, ConvVecCfg::SMEM_BYTES, stream>>>(
+        L.tmW, L.tmY, L.tmY4, L.args);
+    return cudaGetLastError();
+}
+
+template <int OUT, int S>
+static cudaError_t setup_vec_t()
+{
+    return cudaFuncSetAttribute(conv_vec_kernel<OUT, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                ConvVecCfg::SMEM_BYTES);
+}
+
+cudaError_t setup_conv_vec_kernels()
+{
+    cudaError_t e = setup_vec_t<OUT_BF16, 1>();
+    if (e == cudaSuccess) e = setup_vec_t<OUT_F16, 1>();
+    if (e == cudaSuccess) e = setup_vec_t<OUT_F32, 1>();
+    if (e == cudaSuccess) e = setup_vec_t<OUT_BF16, 2>();
+    if (e == cudaSuccess) e = setup_vec_t<OUT_F16, 2>();
+    if (e == cudaSuccess) e = setup_vec_t<OUT_F32, 2>();
+    return e;
+}
+
+cudaError_t launch_conv_vec(const ConvLaunch &L, cudaStream_t stream)
+{
+    const int s = L.args.sw;
+    if (s == 1) {
+        if (L.out == OUT_BF16) return launch_vec_t<OUT_BF16, 1>(L, stream);
+        if (L.out == OUT_F16) return launch_vec_t<OUT_F16, 1>(L, stream);
+        if (L.out == OUT_F32) return launch_vec_t<OUT_F32, 1>(L, stream);
+    } else if (s == 2) {
+        if (L.out == OUT_BF16) return launch_vec_t<OUT_BF16, 2>(L, stream);
+        if (L.out == OUT_F16) return launch_vec_t<OUT_F16, 2>(L, stream);
+        if (L.out == OUT_F32) return launch_vec_t<OUT_F32, 2>(L, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace mmact

@@ -36,6 +36,9 @@ struct ConvArgs {
     int ab_bf16;
     int act;
     float alpha;
+    int vec;             // 1: vectorised producer (conv_vec.cu), 0: per-element gather
+    int TW, TH;          // vectorised path: output tile of TH rows x TW columns (TW * TH = 256)
+    int tiles_oh, tiles_ow, W8;
     int a_tma;           // 1: filter tiles by TMA, 0: gathered by the producer warps
     int y_tma;           // 1: output tiles by TMA store, 0: direct global stores
     int out_elem_bytes;
@@ -48,7 +51,7 @@ struct ConvArgs {
 };
 
 struct ConvLaunch {
-    CUtensorMap tmW, tmY;
+    CUtensorMap tmW, tmY, tmY4;
     ConvArgs args;
     int out;
     int grid;
@@ -58,6 +61,8 @@ struct ConvLaunch {
 // must run with the device current, before the first launch on it.
 cudaError_t setup_gemm_kernels();
 cudaError_t setup_conv_kernels();
+cudaError_t setup_conv_vec_kernels();
+cudaError_t launch_conv_vec(const ConvLaunch &L, cudaStream_t stream);
 cudaError_t launch_gemm(const GemmLaunch &L, cudaStream_t stream);
 cudaError_t launch_conv(const ConvLaunch &L, cudaStream_t stream);
 // out[i] = act(ws[i]) for i < count (ws fp32, out of dtype `out`).

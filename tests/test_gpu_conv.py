@@ -57,6 +57,27 @@ CASES = [
 ]
 
 
+# Geometries that take the vectorised producer (input width a multiple of 8,
+# horizontal stride 1 or 2, filter pitch a multiple of 16 bytes): ragged output
+# rows and columns, several column tiles, exactly-32-wide outputs, asymmetric
+# pads, dilation, fp32 output, ragged channel tiles and K tails.
+VEC_CASES = [
+    (2, 64, 24, 24, 128, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1), "f16", "f16"),
+    (1, 32, 40, 144, 64, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1), "bf16", "bf16"),    # Wo = 144: 3 col tiles
+    (2, 16, 64, 64, 96, 3, 3, (2, 2), (2, 2, 2, 2), (2, 2), "bf16", "bf16"),     # Wo = 32 exactly
+    (2, 24, 64, 64, 200, 1, 1, (2, 2), (0, 0, 0, 0), (1, 1), "bf16", "f32"),     # 1x1 s2, Co ragged
+    (1, 40, 19, 48, 72, 3, 5, (1, 2), (0, 3, 2, 1), (2, 1), "f16", "f32"),       # asymmetric
+    (3, 8, 10, 16, 24, 5, 5, (1, 1), (2, 2, 2, 2), (1, 1), "f16", "bf16"),       # K = 200
+    (1, 16, 7, 16, 16, 3, 3, (2, 1), (1, 1, 2, 2), (1, 2), "bf16", "f16"),       # Wo = 16, Ho = 4
+]
+
+
+@pytest.mark.parametrize("case", VEC_CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}x{c[3]}-{c[4]}k{c[5]}{c[6]}s{c[7][0]}{c[7][1]}")
+@pytest.mark.parametrize("act", ["tanh", "relu"])
+def test_vectorised_geometries(orc, case, act):
+    test_small_geometries(orc, case, act)
+
+
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}x{c[3]}-{c[4]}k{c[5]}{c[6]}s{c[7][0]}{c[7][1]}")
 @pytest.mark.parametrize("act", ["tanh", "leaky_relu"])
 def test_small_geometries(orc, case, act):
