@@ -63,35 +63,29 @@ __device__ __forceinline__ uint4 ldg16(const uint16_t *p)
     return __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
-// Eight output elements e = 0..7 taken from the concatenated chunk words w at
-// element positions SH + S*e.
-template <int S, int SH>
-__device__ __forceinline__ void pick8(const uint32_t *w, uint32_t (&o)[4])
-{
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if constexpr (S == 1) {
-            const int a = SH / 2 + j;
-            o[j] = (SH & 1) ? __byte_perm(w[a], w[a + 1], 0x5432) : w[a];
-        } else {
-            const int a = SH / 2 + 2 * j;
-            o[j] = (SH & 1) ? __byte_perm(w[a], w[a + 1], 0x7632) : __byte_perm(w[a], w[a + 1], 0x5410);
-        }
-    }
-}
-
+// Eight output elements e = 0..7 taken from the concatenated chunk words w
+// (4*NCH words, two 16-bit elements each) at element positions sh + S*e.
+// Branch-free: shift the word array left by sh/2 words with two levels of
+// selects, then build each output word with one byte permute whose selector
+// depends on whether sh is odd.
 template <int S>
-__device__ __forceinline__ void pick8_dispatch(int sh, const uint32_t *w, uint32_t (&o)[4])
+__device__ __forceinline__ void pick8(int sh, const uint32_t *w, uint32_t (&o)[4])
 {
-    switch (sh) {
-    case 0: pick8<S, 0>(w, o); break;
-    case 1: pick8<S, 1>(w, o); break;
-    case 2: pick8<S, 2>(w, o); break;
-    case 3: pick8<S, 3>(w, o); break;
-    case 4: pick8<S, 4>(w, o); break;
-    case 5: pick8<S, 5>(w, o); break;
-    case 6: pick8<S, 6>(w, o); break;
-    default: pick8<S, 7>(w, o); break;
+    constexpr int NW = S == 1 ? 8 : 12;
+    const bool s1 = (sh & 2) != 0, s2 = (sh & 4) != 0, odd = (sh & 1) != 0;
+    uint32_t u[NW - 1], v[NW - 3];
+#pragma unroll
+    for (int i = 0; i < NW - 1; ++i) u[i] = s1 ? w[i + 1] : w[i];
+#pragma unroll
+    for (int i = 0; i < NW - 3; ++i) v[i] = s2 ? u[i + 2] : u[i];
+    if constexpr (S == 1) {
+        const uint32_t sel = odd ? 0x5432u : 0x3210u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = __byte_perm(v[j], v[j + 1], sel);
+    } else {
+        const uint32_t sel = odd ? 0x7632u : 0x5410u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = __byte_perm(v[2 * j], v[2 * j + 1], sel);
     }
 }
 
@@ -246,7 +240,7 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
                             w[4 * c + 3] = ch[i][c].w;
                         }
                         uint32_t o[4];
-                        pick8_dispatch<S>(shift[i], w, o);
+                        pick8<S>(shift[i], w, o);
                         const int kl = gw * ROWS + g + i;
                         ptx::st_shared_v4(bt + (uint32_t)kl * 128u + ((pc8 ^ (uint32_t)(kl & 7)) << 4), o[0],
                                           o[1], o[2], o[3]);
