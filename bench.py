@@ -77,6 +77,23 @@ def traffic_per_launch(kernel, workload):
     return ent.get("dram_bytes_per_launch")
 
 
+# --------------------------------------------------------- multi-rank glue --
+def reduce_max(dist, value, device):
+    """Max of a per-rank scalar over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank, ms_max, world):
+    """Whole-job throughput: every rank runs its own replica (weak scaling), and the
+    job's time is the slowest rank's."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------- clocks --
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
@@ -333,7 +350,9 @@ def run_reference(args):
     wl = synth.WORKLOADS[args.workload]
     inputs = wl.inputs()
     threads = os.cpu_count() or 1
-    n = calibrate_points(oracle_mod, wl, inputs, threads, target_s=2.0)
+    # each step is a bounded sample, sized so the whole run takes about two minutes
+    per_step = min(2.0, max(0.2, 120.0 / (args.steps + args.warmup)))
+    n = calibrate_points(oracle_mod, wl, inputs, threads, target_s=per_step)
     for i in range(args.warmup):
         oracle_sample_run(oracle_mod, wl, inputs, n, threads, seed=100 + i)
     t0 = time.perf_counter()
@@ -416,11 +435,7 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clock_rec = clocks.stop()
-    ms = start.elapsed_time(end) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(dist, start.elapsed_time(end) / args.steps, device)
     st = mmact.mmact_get_last_error()
     if st != mmact.MMACT_OK:
         raise RuntimeError(f"kernel status {mmact.mmact_status_string(st)}")
@@ -448,7 +463,7 @@ def main():
     import oracle as oracle_mod
     parity = parity_spot_check(oracle_mod, prob) if rank == 0 else None
 
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_tflops(flops, ms, world)
     peaks, peak_src = load_peaks()
     if sustained is not None:
         sustained["frac_of_sustained_peak"] = sustained["tflops"] / peaks["bf16_tflops_sustained"]
@@ -525,14 +540,10 @@ def end_to_end(torch, mmact, wl, prob, device, stream, args, flops, world, barri
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms = start.elapsed_time(end) / steps
-    if dist is not None:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(dist, start.elapsed_time(end) / steps, device)
     h2d = sum(t.numel() * t.element_size() for t in hosts)
     d2h = hout.numel() * hout.element_size()
-    return {"value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+    return {"value": job_tflops(flops, ms, world), "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
 
 

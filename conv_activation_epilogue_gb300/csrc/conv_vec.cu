@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
         // issued before any of its byte-picks, and the first group's loads go
         // out before the wait for the ring slot, so load latency overlaps.
         constexpr int ROWS = 64 / Cfg::GATHER_WARPS;     // K rows per warp and stage
-        constexpr int GRP = 4;
+        constexpr int GRP = S == 1 ? 8 : 4;                // rows whose loads are issued together
         const int gw = warp - 6;                         // owns K rows [gw*ROWS, +ROWS) of a stage
         const int HW = p.H * p.W;
         const int taps = p.kh * p.kw;
