@@ -27,7 +27,7 @@ SOURCE = os.path.join(_HERE, "mmact_oracle.c")
 LIBRARY = os.path.join(_HERE, "liboracle.so")
 
 DTYPES = {"f16": 0, "bf16": 1}
-ACTS = {"none": 0, "relu": 1, "leaky_relu": 2, "tanh": 3}
+ACTS = {"none": 0, "relu": 1, "leaky_relu": 2, "tanh": 3, "sigmoid": 4, "gelu": 5}
 
 _build_lock = threading.Lock()
 
@@ -61,6 +61,10 @@ class Oracle:
         L.oracle_decode_bf16.restype = dbl
         L.oracle_tanh.argtypes = [dbl]
         L.oracle_tanh.restype = dbl
+        L.oracle_sigmoid.argtypes = [dbl]
+        L.oracle_sigmoid.restype = dbl
+        L.oracle_gelu.argtypes = [dbl]
+        L.oracle_gelu.restype = dbl
         L.oracle_act.argtypes = [dbl, ci, dbl]
         L.oracle_act.restype = dbl
         L.oracle_conv_out_dim.argtypes = [i64] * 6

@@ -28,7 +28,8 @@
  *        (H + 2p - d(k-1) - 1)/s + 1 extended to asymmetric pads.
  *
  *   act    NONE: z;  RELU: z > 0 ? z : 0;  LEAKY_RELU: z > 0 ? z : alpha*z;
- *          TANH: (e^z - e^-z) / (e^z + e^-z)
+ *          TANH: (e^z - e^-z) / (e^z + e^-z);  SIGMOID: 1 / (1 + e^-z);
+ *          GELU: z/2 * (1 + erf(z / sqrt(2)))
  *     -- LeakyReLU: MatmulLeakyRelu walkthrough, overview formula and its
  *        interface table (the comparison operator was lost when the page was
  *        extracted; read as '>').  ReLU: "ops-nn fused_matmul_relu" article,
@@ -37,6 +38,12 @@
  *        exp(-z), difference over sum).  For |z| > 20 the ratio equals
  *        sign(z) to within fp64 rounding (1 - tanh(20) < 1e-17), so the
  *        oracle returns +-1 there instead of forming inf/inf.
+ *          SIGMOID: 1 / (1 + e^-z)  -- the Fused ConvTanh article's twin operator,
+ *        Fused ConvSigmoid (sigmoid(conv2d)), and the fused_matmul_relu article's
+ *        first fusion family (matmul + ReLU / GELU / Sigmoid / Tanh).
+ *          GELU: z * Phi(z) = z/2 * (1 + erf(z / sqrt(2))) -- same family; the pages
+ *        print no formula, so this is the exact (erf) form, with C's erf() as
+ *        the library step.
  *
  * Input decoding follows the IEEE 754 binary16 definition (1 sign, 5 exponent
  * bits with bias 15, 10 fraction bits) and the bfloat16 definition (the upper
@@ -55,7 +62,8 @@
 #include <string.h>
 
 enum { OR_F16 = 0, OR_BF16 = 1 };
-enum { OR_ACT_NONE = 0, OR_ACT_RELU = 1, OR_ACT_LEAKY_RELU = 2, OR_ACT_TANH = 3 };
+enum { OR_ACT_NONE = 0, OR_ACT_RELU = 1, OR_ACT_LEAKY_RELU = 2, OR_ACT_TANH = 3,
+       OR_ACT_SIGMOID = 4, OR_ACT_GELU = 5 };
 
 /* IEEE 754 binary16 -> double, from the format's definition. */
 double oracle_decode_f16(uint16_t h)
@@ -106,6 +114,16 @@ double oracle_tanh(double z)
     return (ep - em) / (ep + em);
 }
 
+double oracle_sigmoid(double z)
+{
+    return 1.0 / (1.0 + exp(-z));
+}
+
+double oracle_gelu(double z)
+{
+    return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
+}
+
 double oracle_act(double z, int act, double alpha)
 {
     switch (act) {
@@ -113,6 +131,8 @@ double oracle_act(double z, int act, double alpha)
     case OR_ACT_RELU:       return z > 0.0 ? z : 0.0;
     case OR_ACT_LEAKY_RELU: return z > 0.0 ? z : alpha * z;
     case OR_ACT_TANH:       return oracle_tanh(z);
+    case OR_ACT_SIGMOID:    return oracle_sigmoid(z);
+    case OR_ACT_GELU:       return oracle_gelu(z);
     default:                return NAN;
     }
 }

@@ -15,6 +15,7 @@ import math
 import os
 
 import numpy as np
+import scipy.special
 import torch
 import torch.nn.functional as F
 
@@ -48,6 +49,10 @@ def act_ref(z, act, alpha):
         return np.where(z > 0, z, alpha * z)
     if act == "tanh":
         return np.tanh(z)
+    if act == "sigmoid":
+        return scipy.special.expit(z)
+    if act == "gelu":
+        return z * scipy.special.ndtr(z)
     raise ValueError(act)
 
 
@@ -112,6 +117,32 @@ def check_tanh(orc):
     assert float(orc.act([0.75], "tanh")[0]) == orc.tanh(0.75)
 
 
+def check_sigmoid(orc):
+    lib = orc.lib
+    assert lib.oracle_sigmoid(0.0) == 0.5
+    for z in np.concatenate([np.linspace(-40, 40, 801), [1e-9, -3e-7, 700.0, -700.0]]):
+        got = lib.oracle_sigmoid(float(z))
+        assert abs(got - scipy.special.expit(z)) <= 1e-16 + 4e-16 * abs(got), (z, got)
+        # sigma(z) + sigma(-z) = 1 and sigma(z) = (1 + tanh(z/2)) / 2
+        assert abs(got + lib.oracle_sigmoid(float(-z)) - 1.0) <= 5e-16
+        assert abs(got - 0.5 * (1.0 + math.tanh(z / 2))) <= 5e-16
+        assert 0.0 <= got <= 1.0
+    assert float(orc.act([1.5], "sigmoid")[0]) == lib.oracle_sigmoid(1.5)
+
+
+def check_gelu(orc):
+    lib = orc.lib
+    assert lib.oracle_gelu(0.0) == 0.0
+    for z in np.concatenate([np.linspace(-12, 12, 481), [1e-9, -2e-6]]):
+        got = lib.oracle_gelu(float(z))
+        # z * Phi(z), Phi the standard normal CDF (library)
+        assert abs(got - z * scipy.special.ndtr(z)) <= 1e-15 + 4e-15 * abs(got), (z, got)
+        # GELU(z) - GELU(-z) = z (Phi(z) + Phi(-z) = 1)
+        assert abs(got - lib.oracle_gelu(float(-z)) - z) <= 1e-14 * max(1.0, abs(z))
+    assert abs(lib.oracle_gelu(10.0) - 10.0) < 1e-15 and abs(lib.oracle_gelu(-10.0)) < 1e-20
+    assert float(orc.act([0.3], "gelu")[0]) == lib.oracle_gelu(0.3)
+
+
 # -------------------------------------------------------------------- GEMM --
 def _rand_codes(rng, shape, dtype, scale=1.0):
     v = rng.uniform(-scale, scale, size=shape)
@@ -165,7 +196,8 @@ def check_gemm_bruteforce(orc):
     for trial in range(12):
         M, N, K = (int(v) for v in rng.integers(1, 10, size=3))
         dtype = ("f16", "bf16")[trial % 2]
-        act, alpha = [("none", 0), ("relu", 0), ("leaky_relu", 0.2), ("tanh", 0)][trial % 4]
+        act, alpha = [("none", 0), ("relu", 0), ("leaky_relu", 0.2), ("tanh", 0), ("sigmoid", 0),
+                      ("gelu", 0)][trial % 6]
         A = _rand_codes(rng, (M, K), dtype, 2.0)
         B = _rand_codes(rng, (K, N), dtype, 2.0)
         bias = rng.uniform(-1, 1, N).astype(np.float32)
@@ -346,7 +378,7 @@ def check_conv_golden(orc):
 
 
 ALL_CHECKS = [
-    check_decode_f16, check_decode_bf16, check_act_points, check_tanh,
+    check_decode_f16, check_decode_bf16, check_act_points, check_tanh, check_sigmoid, check_gelu,
     check_gemm_identity, check_gemm_permutation, check_gemm_ones, check_gemm_bruteforce,
     check_gemm_points, check_gemm_golden,
     check_conv_shape, check_conv_bruteforce, check_conv_delta, check_conv_as_gemm,

@@ -23,6 +23,9 @@ MUTANTS = {
     "relu passes negatives": ("z > 0.0 ? z : 0.0", "z > 0.0 ? z : 0.5 * z"),
     "tanh numerator sign": ("(ep - em) / (ep + em)", "(em - ep) / (ep + em)"),
     "tanh saturation wrong": ("if (z > 20.0) return 1.0;", "if (z > 2.0) return 1.0;"),
+    "sigmoid exponent sign": ("return 1.0 / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(z));"),
+    "gelu erf scale": ("erf(z / sqrt(2.0))", "erf(z / 2.0)"),
+    "gelu half dropped": ("return 0.5 * z * (1.0 + erf", "return z * (1.0 + erf"),
     "conv dilation dropped (rows)": ("r * g->dh", "r"),
     "conv dilation dropped (cols)": ("q * g->dw", "q"),
     "conv pad sign": ("oh * g->sh - g->pt", "oh * g->sh + g->pt"),
