@@ -107,7 +107,7 @@ bool encode(CUtensorMap *m, mmact_dtype dt, int rank, const void *ptr, const uin
     return r == CUDA_SUCCESS;
 }
 
-bool valid_act(mmact_act a) { return a >= MMACT_ACT_NONE && a <= MMACT_ACT_TANH; }
+bool valid_act(mmact_act a) { return a >= MMACT_ACT_NONE && a <= MMACT_ACT_GELU; }
 bool valid_in(mmact_dtype d) { return d == MMACT_F16 || d == MMACT_BF16; }
 bool valid_out(mmact_dtype d) { return d == MMACT_F16 || d == MMACT_BF16 || d == MMACT_F32; }
 

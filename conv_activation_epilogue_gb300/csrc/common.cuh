@@ -10,7 +10,7 @@
 
 namespace mmact {
 
-enum : int { ACT_NONE = 0, ACT_RELU = 1, ACT_LEAKY = 2, ACT_TANH = 3 };
+enum : int { ACT_NONE = 0, ACT_RELU = 1, ACT_LEAKY = 2, ACT_TANH = 3, ACT_SIGMOID = 4, ACT_GELU = 5 };
 enum : int { OUT_F32 = 0, OUT_F16 = 1, OUT_BF16 = 2 };
 
 // Bits of the per-device status word.
@@ -27,12 +27,27 @@ __device__ __forceinline__ float tanh_f32(float z)
     return copysignf(__fdividef(1.0f - e, 1.0f + e), z);
 }
 
+// 1 / (1 + e^-z); for very negative z the denominator overflows to +inf and
+// the fast division returns 0, the correct limit.
+__device__ __forceinline__ float sigmoid_f32(float z)
+{
+    return __fdividef(1.0f, 1.0f + __expf(-z));
+}
+
+// z * Phi(z) = z/2 * (1 + erf(z / sqrt(2))), with the CUDA math library's erff.
+__device__ __forceinline__ float gelu_f32(float z)
+{
+    return 0.5f * z * (1.0f + erff(z * 0.7071067811865476f));
+}
+
 template <int ACT>
 __device__ __forceinline__ float act_f32(float z, float alpha)
 {
     if constexpr (ACT == ACT_RELU) return z > 0.0f ? z : 0.0f;
     else if constexpr (ACT == ACT_LEAKY) return z > 0.0f ? z : alpha * z;
     else if constexpr (ACT == ACT_TANH) return tanh_f32(z);
+    else if constexpr (ACT == ACT_SIGMOID) return sigmoid_f32(z);
+    else if constexpr (ACT == ACT_GELU) return gelu_f32(z);
     else return z;
 }
 
@@ -181,6 +196,12 @@ __device__ __forceinline__ void epi_unit_dispatch(int act, uint32_t taddr, const
         break;
     case ACT_TANH:
         epi_unit<OUT, ACT_TANH, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        break;
+    case ACT_SIGMOID:
+        epi_unit<OUT, ACT_SIGMOID, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        break;
+    case ACT_GELU:
+        epi_unit<OUT, ACT_GELU, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
         break;
     default:
         epi_unit<OUT, ACT_NONE, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);

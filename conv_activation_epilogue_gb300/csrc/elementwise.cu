@@ -94,6 +94,8 @@ static cudaError_t launch_act_o(const float *ws, void *out, int64_t count, int a
     case ACT_RELU: act_kernel<OUT, ACT_RELU><<<grid, 256, 0, s>>>(ws, out, count, alpha); break;
     case ACT_LEAKY: act_kernel<OUT, ACT_LEAKY><<<grid, 256, 0, s>>>(ws, out, count, alpha); break;
     case ACT_TANH: act_kernel<OUT, ACT_TANH><<<grid, 256, 0, s>>>(ws, out, count, alpha); break;
+    case ACT_SIGMOID: act_kernel<OUT, ACT_SIGMOID><<<grid, 256, 0, s>>>(ws, out, count, alpha); break;
+    case ACT_GELU: act_kernel<OUT, ACT_GELU><<<grid, 256, 0, s>>>(ws, out, count, alpha); break;
     default: act_kernel<OUT, ACT_NONE><<<grid, 256, 0, s>>>(ws, out, count, alpha); break;
     }
     return cudaGetLastError();
@@ -120,6 +122,8 @@ static cudaError_t launch_bias_act_o(const float *bias, void *out, int64_t rows,
     case ACT_RELU: MMACT_BA(ACT_RELU); break;
     case ACT_LEAKY: MMACT_BA(ACT_LEAKY); break;
     case ACT_TANH: MMACT_BA(ACT_TANH); break;
+    case ACT_SIGMOID: MMACT_BA(ACT_SIGMOID); break;
+    case ACT_GELU: MMACT_BA(ACT_GELU); break;
     default: MMACT_BA(ACT_NONE); break;
     }
 #undef MMACT_BA

@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(_HERE, "libmmact.so")
 
 MMACT_OK, MMACT_ERR_INVALID_ARG, MMACT_ERR_UNSUPPORTED, MMACT_ERR_CUDA, MMACT_ERR_TIMEOUT = range(5)
-ACT = {"none": 0, "relu": 1, "leaky_relu": 2, "tanh": 3}
+ACT = {"none": 0, "relu": 1, "leaky_relu": 2, "tanh": 3, "sigmoid": 4, "gelu": 5}
 DTYPE = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
 
 _lib = None

@@ -26,6 +26,11 @@
  *   MMACT_ACT_RELU        z > 0 ? z : 0
  *   MMACT_ACT_LEAKY_RELU  z > 0 ? z : alpha * z
  *   MMACT_ACT_TANH        (e^z - e^-z) / (e^z + e^-z)
+ *   MMACT_ACT_SIGMOID     1 / (1 + e^-z)       (the Fused ConvTanh article's twin
+ *                         operator, Fused ConvSigmoid)
+ *   MMACT_ACT_GELU        z/2 * (1 + erf(z / sqrt(2)))   (the fused_matmul_relu
+ *                         article's matmul + GELU / Sigmoid / Tanh family; exact
+ *                         erf form, the pages print no formula)
  *
  * Conventions for every entry point
  *   - Tensor pointers are DEVICE pointers (cudaMalloc / torch CUDA memory) on
@@ -66,7 +71,9 @@ typedef enum {
     MMACT_ACT_NONE = 0,
     MMACT_ACT_RELU = 1,
     MMACT_ACT_LEAKY_RELU = 2,
-    MMACT_ACT_TANH = 3
+    MMACT_ACT_TANH = 3,
+    MMACT_ACT_SIGMOID = 4,
+    MMACT_ACT_GELU = 5
 } mmact_act;
 
 typedef enum {

@@ -100,7 +100,7 @@ def test_gemm_host_validation(lib):
     assert gemm(lib, ab=2) == E             # fp32 operands are not a kind::f16 input
     assert gemm(lib, ab=7) == E
     assert gemm(lib, cd=5) == E
-    assert gemm(lib, act=4) == E
+    assert gemm(lib, act=6) == E
     assert gemm(lib, act=-1) == E
     assert gemm(lib, bias=P16 + 1) == E     # bias must be 4-byte aligned
     assert gemm(lib, A=P_MIS) == U

@@ -73,13 +73,13 @@ VEC_CASES = [
 
 
 @pytest.mark.parametrize("case", VEC_CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}x{c[3]}-{c[4]}k{c[5]}{c[6]}s{c[7][0]}{c[7][1]}")
-@pytest.mark.parametrize("act", ["tanh", "relu"])
+@pytest.mark.parametrize("act", ["tanh", "relu", "sigmoid", "gelu"])
 def test_vectorised_geometries(orc, case, act):
     test_small_geometries(orc, case, act)
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}x{c[3]}-{c[4]}k{c[5]}{c[6]}s{c[7][0]}{c[7][1]}")
-@pytest.mark.parametrize("act", ["tanh", "leaky_relu"])
+@pytest.mark.parametrize("act", ["tanh", "leaky_relu", "sigmoid", "gelu"])
 def test_small_geometries(orc, case, act):
     Nb, C, H, W, Co, kh, kw, stride, pads, dil, dt, od = case
     rng = np.random.default_rng(Nb * 1000 + C * 10 + Co)

@@ -63,7 +63,8 @@ def test_small_shapes_all_tiles(orc, tile_n, shape):
     rng = np.random.default_rng(M * 7 + N * 13 + K + tile_n)
     mmact.mmact_set_gemm_tile_n(tile_n)
     for ab, cd, act, alpha in [("bf16", "bf16", "leaky_relu", 0.2), ("f16", "f32", "relu", 0.0),
-                               ("bf16", "f16", "tanh", 0.0), ("f16", "bf16", "none", 0.0)]:
+                               ("bf16", "f16", "tanh", 0.0), ("f16", "bf16", "none", 0.0),
+                               ("bf16", "f32", "sigmoid", 0.0), ("f16", "bf16", "gelu", 0.0)]:
         A = rand_codes(rng, (M, K), ab)
         B = rand_codes(rng, (K, N), ab)
         bias = rng.uniform(-1, 1, N).astype(np.float32)
@@ -74,7 +75,7 @@ def test_small_shapes_all_tiles(orc, tile_n, shape):
 
 
 @pytest.mark.parametrize("shape", [(200, 136, 72), (384, 256, 1024)], ids=lambda s: "x".join(map(str, s)))
-@pytest.mark.parametrize("act", ["relu", "leaky_relu", "tanh", "none"])
+@pytest.mark.parametrize("act", ["relu", "leaky_relu", "tanh", "none", "sigmoid", "gelu"])
 def test_split_matches_oracle_and_workspace_holds_z(orc, shape, act):
     M, N, K = shape
     rng = np.random.default_rng(5 + M)
@@ -100,7 +101,7 @@ def test_empty_contraction_gives_act_of_bias(orc):
     bias = rng.uniform(-2, 2, 24).astype(np.float32)
     A = np.zeros((5, 0), dtype=np.uint16)
     B = np.zeros((0, 24), dtype=np.uint16)
-    for act in ("relu", "leaky_relu", "tanh"):
+    for act in ("relu", "leaky_relu", "tanh", "sigmoid", "gelu"):
         dA = torch.empty((5, 0), dtype=torch.bfloat16, device="cuda")
         dB = torch.empty((0, 24), dtype=torch.bfloat16, device="cuda")
         C = torch.full((5, 24), float("nan"), dtype=torch.float32, device="cuda")
