@@ -89,9 +89,9 @@ CUtensorMapDataType tmap_type(mmact_dtype d)
 }
 
 // Tiled map over a row-major tensor given innermost-first dims (elements) and
-// the byte strides of dims 1..rank-1, with a 128-byte swizzle.
+// the byte strides of dims 1..rank-1, with a 128-byte swizzle (or none).
 bool encode(CUtensorMap *m, mmact_dtype dt, int rank, const void *ptr, const uint64_t *dims,
-            const uint64_t *strides_bytes, const uint32_t *box)
+            const uint64_t *strides_bytes, const uint32_t *box, bool swizzle = true)
 {
     cuuint64_t gd[5], gs[4];
     cuuint32_t bx[5], es[5];
@@ -102,7 +102,8 @@ bool encode(CUtensorMap *m, mmact_dtype dt, int rank, const void *ptr, const uin
     }
     for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
     CUresult r = g_encode(m, tmap_type(dt), (cuuint32_t)rank, const_cast<void *>(ptr), gd, gs, bx, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -112,6 +113,29 @@ bool valid_in(mmact_dtype d) { return d == MMACT_F16 || d == MMACT_BF16; }
 bool valid_out(mmact_dtype d) { return d == MMACT_F16 || d == MMACT_BF16 || d == MMACT_F32; }
 
 constexpr int64_t MAX_DIM = (int64_t(1) << 31) - 1;
+
+// Output tile width for a GEMM: the candidate with the least estimated time
+// = (waves of persistent tiles over the SMs) x (tile width) / (throughput of
+// that width relative to 256).  The relative throughputs were measured on
+// GB300 at 8192^3 (one CTA per SM, 128-row tiles): 1757, 1443, 1397, 1133 and
+// 576 TFLOP/s for widths 256, 224, 192, 128 and 64.  Ties go to the wider tile.
+int choose_tile_n(int64_t tiles_m, int64_t N, int sms)
+{
+    static const int widths[] = {256, 224, 192, 128, 64};
+    static const double rel_rate[] = {1.0, 0.82, 0.80, 0.61, 0.32};
+    int best = 256;
+    double best_cost = 1e300;
+    for (int i = 0; i < 5; ++i) {
+        const int64_t tiles = tiles_m * ((N + widths[i] - 1) / widths[i]);
+        const int64_t waves = (tiles + sms - 1) / sms;
+        const double cost = (double)waves * widths[i] / rel_rate[i];
+        if (cost < best_cost * 0.999) {
+            best_cost = cost;
+            best = widths[i];
+        }
+    }
+    return best;
+}
 
 // Shared by mmact_gemm and the first kernel of mmact_gemm_split.
 mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void *C, int64_t M,
@@ -129,12 +153,7 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
     std::memset(&L, 0, sizeof(L));
     const int tiles_m = (int)((M + 127) / 128);
     int bn = g_tile_n.load();
-    if (bn == 0) {
-        // Widest tile that still gives every SM at least one tile.
-        const int64_t t256 = tiles_m * ((N + 255) / 256);
-        const int64_t t128 = tiles_m * ((N + 127) / 128);
-        bn = t256 >= dev->sm_count ? 256 : (t128 >= dev->sm_count ? 128 : 64);
-    }
+    if (bn == 0) bn = choose_tile_n(tiles_m, N, dev->sm_count);
     const int tiles_n = (int)((N + bn - 1) / bn);
     GemmArgs &a = L.args;
     a.M = (int)M;
@@ -165,6 +184,10 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
     if (!encode(&L.tmA, ab, 2, A, dA, sA, bA) || !encode(&L.tmB, ab, 2, B, dB, sB, bB) ||
         !encode(&L.tmC, cd, 2, C, dC, sC, bC))
         return MMACT_ERR_CUDA;
+    if (bn == 224 && ce == 2) {
+        const uint32_t bT[2] = {32, 32};
+        if (!encode(&L.tmCt, cd, 2, C, dC, sC, bT, false)) return MMACT_ERR_CUDA;
+    }
     return launch_gemm(L, stream) == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
 }
 
@@ -449,7 +472,9 @@ MMACT_EXPORT mmact_status mmact_selftest_wait_timeout(uint64_t timeout_ns, void 
 
 MMACT_EXPORT mmact_status mmact_set_gemm_tile_n(int tile_n)
 {
-    if (tile_n != 0 && tile_n != 64 && tile_n != 128 && tile_n != 256) return MMACT_ERR_INVALID_ARG;
+    if (tile_n != 0 && tile_n != 64 && tile_n != 128 && tile_n != 192 && tile_n != 224 &&
+        tile_n != 256)
+        return MMACT_ERR_INVALID_ARG;
     g_tile_n.store(tile_n);
     return MMACT_OK;
 }

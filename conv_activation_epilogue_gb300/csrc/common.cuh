@@ -94,17 +94,28 @@ __device__ __forceinline__ bool pipe_wait(const Pipe &pp, uint32_t bar, uint32_t
 //   B stage: [64 K x BN] MN-major, 128-byte swizzle, BN/64 column chunks of
 //            64 K rows x 128 B each (chunk stride 8192 B); the K step of 16
 //            moves 16 rows = 2048 bytes.
+// Tile geometry shared by the producer, MMA issuer and epilogue: BN columns
+// per tile, stored as ceil(BN/64) chunks of 64 columns; the two TMEM
+// accumulator buffers start 256 columns apart when BN > 128 (BN apart below).
+template <int BN>
+struct TileN {
+    static constexpr int NCHUNK = (BN + 63) / 64;
+    static constexpr uint32_t B_BYTES = 64u * 64u * 2u * NCHUNK;
+    static constexpr uint32_t ACC_STRIDE = BN > 128 ? 256u : (uint32_t)BN;
+    static constexpr uint32_t TMEM_COLS = 2u * ACC_STRIDE;
+};
+
 template <int BN, int STAGES>
 __device__ void mma_role(const Pipe &pp, uint32_t sA, uint32_t sB, int num_tiles, int num_kb,
                          uint32_t idesc)
 {
-    constexpr uint32_t A_BYTES = 128 * 64 * 2, B_BYTES = 64 * BN * 2;
+    constexpr uint32_t A_BYTES = 128 * 64 * 2, B_BYTES = TileN<BN>::B_BYTES;
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         if (!pipe_wait(pp, pp.tempty0 + 8 * acc, acc_phase ^ 1u)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint32_t d = pp.tmem + acc * BN;
+        const uint32_t d = pp.tmem + acc * TileN<BN>::ACC_STRIDE;
         for (int kb = 0; kb < num_kb; ++kb) {
             if (!pipe_wait(pp, pp.full0 + 8 * stage, phase)) { ok = false; break; }
             ptx::tc_fence_after();
@@ -136,21 +147,42 @@ __device__ void mma_role(const Pipe &pp, uint32_t sA, uint32_t sB, int num_tiles
 // applies the activation in fp32, converts, and writes the row into a
 // 32 x 128 B shared buffer in the 128-byte swizzled order a TMA store expects
 // (16-byte chunk c of row r lands at chunk c ^ (r & 7)).
-template <int OUT, int ACT, bool BIAS_ROW>
+//
+// NCOL = 32 with a 16-bit output is the narrow tail unit of a 224-wide tile:
+// 64-byte rows, written densely without swizzle (its TMA store uses an
+// unswizzled map).
+template <int OUT, int ACT, bool BIAS_ROW, int NCOL = (OUT == OUT_F32 ? 32 : 64)>
 __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, int nvalid,
                                          float brow, float alpha, uint32_t buf, int lane)
 {
-    constexpr int COLS = OUT == OUT_F32 ? 32 : 64;
+    constexpr int COLS = NCOL;
+    constexpr bool WIDE = COLS == 64;                  // two TMEM loads per unit
     uint32_t r0[32];
     uint32_t r1[32];
     ptx::tmem_ld32(taddr, r0);
-    if constexpr (OUT != OUT_F32) ptx::tmem_ld32(taddr + 32, r1);
+    if constexpr (WIDE) ptx::tmem_ld32(taddr + 32, r1);
     float bc[COLS];
 #pragma unroll
     for (int j = 0; j < COLS; ++j)
         bc[j] = BIAS_ROW ? brow : ((bias_col != nullptr && j < nvalid) ? __ldg(bias_col + j) : 0.0f);
     ptx::tmem_ld_wait(r0);
-    if constexpr (OUT != OUT_F32) ptx::tmem_ld_wait(r1);
+    if constexpr (WIDE) ptx::tmem_ld_wait(r1);
+    if constexpr (OUT != OUT_F32 && !WIDE) {
+        // 32 columns of a 16-bit output: 4 chunks of 16 bytes, row pitch 64 bytes
+        const uint32_t row = buf + (uint32_t)lane * 64u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int col = 8 * c + 2 * e;
+                w[e] = pack2<OUT>(act_f32<ACT>(__uint_as_float(r0[col]) + bc[col], alpha),
+                                  act_f32<ACT>(__uint_as_float(r0[col + 1]) + bc[col + 1], alpha));
+            }
+            ptx::st_shared_v4(row + (uint32_t)c * 16u, w[0], w[1], w[2], w[3]);
+        }
+        return;
+    }
     const uint32_t row = buf + (uint32_t)lane * 128u;
     const uint32_t sw = (uint32_t)(lane & 7);
     if constexpr (OUT == OUT_F32) {
@@ -182,29 +214,29 @@ __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, 
     }
 }
 
-template <int OUT, bool BIAS_ROW>
+template <int OUT, bool BIAS_ROW, int NCOL = (OUT == OUT_F32 ? 32 : 64)>
 __device__ __forceinline__ void epi_unit_dispatch(int act, uint32_t taddr, const float *bias_col,
                                                   int nvalid, float brow, float alpha, uint32_t buf,
                                                   int lane)
 {
     switch (act) {
     case ACT_RELU:
-        epi_unit<OUT, ACT_RELU, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        epi_unit<OUT, ACT_RELU, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
         break;
     case ACT_LEAKY:
-        epi_unit<OUT, ACT_LEAKY, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        epi_unit<OUT, ACT_LEAKY, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
         break;
     case ACT_TANH:
-        epi_unit<OUT, ACT_TANH, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        epi_unit<OUT, ACT_TANH, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
         break;
     case ACT_SIGMOID:
-        epi_unit<OUT, ACT_SIGMOID, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        epi_unit<OUT, ACT_SIGMOID, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
         break;
     case ACT_GELU:
-        epi_unit<OUT, ACT_GELU, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        epi_unit<OUT, ACT_GELU, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
         break;
     default:
-        epi_unit<OUT, ACT_NONE, BIAS_ROW>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        epi_unit<OUT, ACT_NONE, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
         break;
     }
 }

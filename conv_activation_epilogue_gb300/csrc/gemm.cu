@@ -31,11 +31,14 @@ template <int BN>
 struct GemmCfg {
     static constexpr int BM = 128, BK = 64;
     static constexpr int A_BYTES = BM * BK * 2;                  // 16 KB
-    static constexpr int B_BYTES = BK * BN * 2;                  // BN/64 chunks of 8 KB
+    static constexpr int B_BYTES = (int)TileN<BN>::B_BYTES;      // ceil(BN/64) chunks of 8 KB
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
     static constexpr int EPI_BYTES = 4 * 2 * 4096;               // 4 warps x 2 x (32 x 128 B)
-    static constexpr int TMEM_COLS = 2 * BN;
+    // as many stages as fit next to the epilogue staging buffers
+    static constexpr int STAGES = (232448 - EPI_BYTES - 256) / STAGE_BYTES > 8
+                                      ? 8
+                                      : (232448 - EPI_BYTES - 256) / STAGE_BYTES;
+    static constexpr int TMEM_COLS = (int)TileN<BN>::TMEM_COLS;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
@@ -57,10 +60,13 @@ __device__ __forceinline__ void gemm_tile(int t, const GemmArgs &p, int &mb, int
     nb = r / gm;
 }
 
+// tmCt: the map for the 32-column tail unit of a 224-wide tile with a 16-bit
+// output (unswizzled 64-byte rows); unused otherwise.
 template <int BN, int OUT>
 __global__ void __launch_bounds__(192, 1)
     gemm_act_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, const GemmArgs p)
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmCt,
+                    const GemmArgs p)
 {
     using Cfg = GemmCfg<BN>;
     constexpr int STAGES = Cfg::STAGES;
@@ -124,7 +130,7 @@ __global__ void __launch_bounds__(192, 1)
                     ptx::mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
                     ptx::tma_load_2d(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * 64, mb * 128);
 #pragma unroll
-                    for (int c = 0; c < BN / 64; ++c)
+                    for (int c = 0; c < TileN<BN>::NCHUNK; ++c)
                         ptx::tma_load_2d(sB + stage * Cfg::B_BYTES + c * 8192, &tmB, fb,
                                          nb * BN + c * 64, kb * 64);
                     issued |= 1u << stage;
@@ -158,7 +164,7 @@ __global__ void __launch_bounds__(192, 1)
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) { ok = false; break; }
             ptx::tc_fence_after();
-            const uint32_t tbase = pp.tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+            const uint32_t tbase = pp.tmem + ((uint32_t)(q * 32) << 16) + acc * TileN<BN>::ACC_STRIDE;
             const int row0 = mb * 128 + q * 32;
 #pragma unroll 1
             for (int u = 0; u < BN / COLS; ++u) {
@@ -173,6 +179,23 @@ __global__ void __launch_bounds__(192, 1)
                 __syncwarp();
                 if (lane == 0 && row0 < p.M && col0 < p.N) {
                     ptx::tma_store_2d(&tmC, buf, col0, row0);
+                    ptx::bulk_commit();
+                }
+            }
+            if constexpr (BN % COLS != 0) {
+                // tail: the last 32 columns of a 224-wide tile (16-bit output)
+                static_assert(BN % COLS == 32 && OUT != OUT_F32, "tail unit is 32 16-bit columns");
+                const uint32_t buf = my_buf + (units++ & 1u) * 4096u;
+                if (lane == 0) ptx::bulk_wait_read<1>();
+                __syncwarp();
+                const int col0 = n0 + (BN / COLS) * COLS;
+                epi_unit_dispatch<OUT, false, 32>(p.act, tbase + (BN / COLS) * COLS,
+                                                  p.bias != nullptr ? p.bias + col0 : nullptr,
+                                                  p.N - col0, 0.0f, p.alpha, buf, lane);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && row0 < p.M && col0 < p.N) {
+                    ptx::tma_store_2d(&tmCt, buf, col0, row0);
                     ptx::bulk_commit();
                 }
             }
@@ -199,7 +222,7 @@ template <int BN, int OUT>
 static cudaError_t launch_gemm_t(const GemmLaunch &L, cudaStream_t stream)
 {
     gemm_act_kernel<BN, OUT><<<L.grid, 192, GemmCfg<BN>::SMEM_BYTES, stream>>>(L.tmA, L.tmB, L.tmC,
-                                                                                L.args);
+                                                                                L.tmCt, L.args);
     return cudaGetLastError();
 }
 
@@ -215,6 +238,12 @@ cudaError_t setup_gemm_kernels()
     cudaError_t e = cudaSuccess;
 #define MMACT_GEMM_SETUP(BN_, OUT_) \
     if (e == cudaSuccess) e = setup_gemm_t<BN_, OUT_>();
+    MMACT_GEMM_SETUP(224, OUT_BF16)
+    MMACT_GEMM_SETUP(224, OUT_F16)
+    MMACT_GEMM_SETUP(224, OUT_F32)
+    MMACT_GEMM_SETUP(192, OUT_BF16)
+    MMACT_GEMM_SETUP(192, OUT_F16)
+    MMACT_GEMM_SETUP(192, OUT_F32)
     MMACT_GEMM_SETUP(256, OUT_BF16)
     MMACT_GEMM_SETUP(256, OUT_F16)
     MMACT_GEMM_SETUP(256, OUT_F32)
@@ -232,6 +261,12 @@ cudaError_t launch_gemm(const GemmLaunch &L, cudaStream_t stream)
 {
 #define MMACT_GEMM_CASE(BN_, OUT_) \
     if (L.tile_n == BN_ && L.out == OUT_) return launch_gemm_t<BN_, OUT_>(L, stream);
+    MMACT_GEMM_CASE(224, OUT_BF16)
+    MMACT_GEMM_CASE(224, OUT_F16)
+    MMACT_GEMM_CASE(224, OUT_F32)
+    MMACT_GEMM_CASE(192, OUT_BF16)
+    MMACT_GEMM_CASE(192, OUT_F16)
+    MMACT_GEMM_CASE(192, OUT_F32)
     MMACT_GEMM_CASE(256, OUT_BF16)
     MMACT_GEMM_CASE(256, OUT_F16)
     MMACT_GEMM_CASE(256, OUT_F32)

@@ -20,9 +20,9 @@ struct GemmArgs {
 };
 
 struct GemmLaunch {
-    CUtensorMap tmA, tmB, tmC;
+    CUtensorMap tmA, tmB, tmC, tmCt;   // tmCt: 32-column tail store map (224-wide tiles)
     GemmArgs args;
-    int tile_n;          // 64, 128 or 256
+    int tile_n;          // 64, 128, 192, 224 or 256
     int out;             // OUT_*
     int grid;
 };

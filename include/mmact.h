@@ -214,8 +214,8 @@ void mmact_set_wait_timeout_ns(uint64_t ns);
 mmact_status mmact_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
 
 /*
- * Tuning and testing aid: force the N-extent of the GEMM output tile (64, 128
- * or 256; 0 = automatic choice).  Applies to later mmact_gemm* calls in the
+ * Tuning and testing aid: force the N-extent of the GEMM output tile (64, 128,
+ * 192, 224 or 256; 0 = automatic choice).  Applies to later mmact_gemm* calls in the
  * process.  Returns MMACT_ERR_INVALID_ARG for other values.
  */
 mmact_status mmact_set_gemm_tile_n(int tile_n);

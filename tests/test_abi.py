@@ -49,7 +49,7 @@ def test_version_and_status_strings(lib):
 def test_tile_override_validation(lib):
     for bad in (1, 32, 96, 512, -64):
         assert lib.mmact_set_gemm_tile_n(bad) == mmact.MMACT_ERR_INVALID_ARG
-    for good in (64, 128, 256, 0):
+    for good in (64, 128, 192, 224, 256, 0):
         assert lib.mmact_set_gemm_tile_n(good) == mmact.MMACT_OK
 
 

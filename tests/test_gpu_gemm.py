@@ -56,7 +56,7 @@ SMALL = [  # (M, N, K)
 ]
 
 
-@pytest.mark.parametrize("tile_n", [64, 128, 256])
+@pytest.mark.parametrize("tile_n", [64, 128, 192, 224, 256])
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
 def test_small_shapes_all_tiles(orc, tile_n, shape):
     M, N, K = shape
