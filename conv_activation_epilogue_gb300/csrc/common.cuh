@@ -18,20 +18,20 @@ enum : unsigned { ST_TIMEOUT = 1u, ST_SMEM_ALIGN = 2u };
 
 constexpr uint64_t DRAIN_NS = 1000000000ull;   // bound on end-of-kernel drains
 
-// tanh(z) as the ratio of exponentials (e^z - e^-z) / (e^z + e^-z), with
-// numerator and denominator multiplied by e^-|z| so that nothing overflows:
-// tanh(|z|) = (1 - e^{-2|z|}) / (1 + e^{-2|z|}), sign restored last.
+// tanh in fp32 with the hardware's tanh.approx.f32 (one MUFU operation; the
+// ratio-of-exponentials form (e^z - e^-z)/(e^z + e^-z) would take two, an
+// exponential and a reciprocal).  Its relative error, about 2^-11, is well
+// inside the output tolerance; it saturates to +-1 without overflow.
 __device__ __forceinline__ float tanh_f32(float z)
 {
-    const float e = __expf(-2.0f * fabsf(z));
-    return copysignf(__fdividef(1.0f - e, 1.0f + e), z);
+    return ptx::tanh_approx(z);
 }
 
-// 1 / (1 + e^-z); for very negative z the denominator overflows to +inf and
-// the fast division returns 0, the correct limit.
+// 1 / (1 + e^-z) = (1 + tanh(z/2)) / 2: one MUFU operation, absolute error
+// about 2^-12, saturating to 0 and 1.
 __device__ __forceinline__ float sigmoid_f32(float z)
 {
-    return __fdividef(1.0f, 1.0f + __expf(-z));
+    return fmaf(0.5f, ptx::tanh_approx(0.5f * z), 0.5f);
 }
 
 // z * Phi(z) = z/2 * (1 + erf(z / sqrt(2))), with the CUDA math library's erff.
@@ -83,6 +83,13 @@ __device__ __forceinline__ void pipe_fail(const Pipe &pp)
 __device__ __forceinline__ bool pipe_wait(const Pipe &pp, uint32_t bar, uint32_t parity)
 {
     return ptx::mbar_wait_bounded(bar, parity, pp.wait_ns, pp.abort);
+}
+
+// The epilogue's wait for a finished accumulator: long, and not on the
+// critical path, so the waiting warps are parked between polls.
+__device__ __forceinline__ bool epi_wait(const Pipe &pp, uint32_t bar, uint32_t parity)
+{
+    return ptx::mbar_wait_bounded(bar, parity, pp.wait_ns, pp.abort, 1000);
 }
 
 // The MMA issuer (one thread).  For every tile of this CTA it waits for a free

@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cta_sync();
     ptx::tc_fence_after();
     pp.tmem = misc[0];
 
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
             const int co = co_row0 + lane;
             const float brow = (p.bias != nullptr && co < p.Co) ? __ldg(p.bias + co) : 0.0f;
             uint32_t got = 1;
-            if (lane == 0) got = pipe_wait(pp, pp.tfull0 + 8 * acc, acc_phase) ? 1u : 0u;
+            if (lane == 0) got = epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase) ? 1u : 0u;
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) { ok = false; break; }
             ptx::tc_fence_after();
@@ -276,8 +276,13 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
         __syncwarp();
     }
 
+    // Every role must be done before TMEM is released.  In the producer and
+    // MMA warps only lane 0 ran the role loop, so the warps arrive here
+    // diverged: the thread-counting barrier waits for every thread, where the
+    // warp-counting bar.sync behind __syncthreads() could complete early.
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cta_sync();
+    __syncwarp();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(pp.tmem, Cfg::TMEM_COLS);

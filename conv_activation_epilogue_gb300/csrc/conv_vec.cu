@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cta_sync();
     ptx::tc_fence_after();
     pp.tmem = misc[0];
 
@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
         // out before the wait for the ring slot, so load latency overlaps.
         constexpr int ROWS = 64 / Cfg::GATHER_WARPS;     // K rows per warp and stage
         constexpr int GRP = S == 1 ? 8 : 4;                // rows whose loads are issued together
+        static_assert(ROWS <= 32 && ROWS % GRP == 0, "row split");
         const int gw = warp - 6;                         // owns K rows [gw*ROWS, +ROWS) of a stage
         const int HW = p.H * p.W;
         const int taps = p.kh * p.kw;
@@ -190,15 +191,27 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
             int n, toh, tow, cb;
             vconv_tile(t, p, n, toh, tow, cb);
             const int oh = toh * p.TH + t_row;
-            const int ihb = oh * p.sh - p.pt;
+            const int ihb = oh * p.sh - p.pt;            // input row of tap r = 0
             const int iwb = (tow * p.TW + t_vec * 8) * S - p.pl;
+            const int ihbW = ihb * p.W;
             const uint16_t *xn = p.x + (int64_t)n * p.C * HW;
             for (int kb = 0; kb < p.num_kb; ++kb) {
-                int k = kb * 64 + gw * ROWS;
-                int ci = k / taps;
-                int rem = k - ci * taps;
-                int r = rem / p.kw;
-                int q = rem - r * p.kw;
+                // Lanes 0..ROWS-1 decode this warp's K rows k = (ci, r, q) in
+                // parallel; each row's offsets are then broadcast by shuffles,
+                // so the row loop below has no divisions and no branches.  A
+                // row past K gets an r*dh that puts every lane out of range.
+                int my_rowoff = 0, my_rdh = 1 << 28, my_qdw = 0;
+                if (lane < ROWS) {
+                    const int k = kb * 64 + gw * ROWS + lane;
+                    if (k < p.K) {
+                        const int ci = k / taps;
+                        const int tap = k - ci * taps;
+                        const int r = tap / p.kw;
+                        my_rdh = r * p.dh;
+                        my_qdw = (tap - r * p.kw) * p.dw;
+                        my_rowoff = ci * HW + my_rdh * p.W;
+                    }
+                }
                 const uint32_t bt = sB + stage * Cfg::B_BYTES + lane_off;
 #pragma unroll 1
                 for (int g = 0; g < ROWS; g += GRP) {
@@ -206,21 +219,18 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
                     int shift[GRP];
 #pragma unroll
                     for (int i = 0; i < GRP; ++i) {
-                        const int ih = ihb + r * p.dh;
-                        const int iws = iwb + q * p.dw;
+                        const int rowoff = __shfl_sync(0xffffffffu, my_rowoff, g + i);
+                        const int rdh = __shfl_sync(0xffffffffu, my_rdh, g + i);
+                        const int qdw = __shfl_sync(0xffffffffu, my_qdw, g + i);
+                        const bool rowok = (unsigned)(ihb + rdh) < (unsigned)p.H;
+                        const int iws = iwb + qdw;
                         const int c0 = iws >> 3;                 // floor(iws / 8)
-                        const bool rowok = k < p.K && (unsigned)ih < (unsigned)p.H;
-                        const uint16_t *rowp = xn + ci * HW + ih * p.W;
+                        const int e0 = rowoff + ihbW + c0 * 8;   // element offset of chunk c0
                         shift[i] = iws & 7;
 #pragma unroll
                         for (int c = 0; c < NCH; ++c) {
                             ch[i][c] = make_uint4(0u, 0u, 0u, 0u);
-                            if (rowok && (unsigned)(c0 + c) < (unsigned)p.W8) ch[i][c] = ldg16(rowp + (c0 + c) * 8);
-                        }
-                        ++k;
-                        if (++q == p.kw) {
-                            q = 0;
-                            if (++r == p.kh) { r = 0; ++ci; }
+                            if (rowok && (unsigned)(c0 + c) < (unsigned)p.W8) ch[i][c] = ldg16(xn + e0 + c * 8);
                         }
                     }
                     if (g == 0) {
@@ -267,7 +277,7 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
             const int co = co_row0 + lane;
             const float brow = (p.bias != nullptr && co < p.Co) ? __ldg(p.bias + co) : 0.0f;
             uint32_t got = 1;
-            if (lane == 0) got = pipe_wait(pp, pp.tfull0 + 8 * acc, acc_phase) ? 1u : 0u;
+            if (lane == 0) got = epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase) ? 1u : 0u;
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) { ok = false; break; }
             ptx::tc_fence_after();
@@ -310,8 +320,13 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
         __syncwarp();
     }
 
+    // Every role must be done before TMEM is released.  In the producer and
+    // MMA warps only lane 0 ran the role loop, so the warps arrive here
+    // diverged: the thread-counting barrier waits for every thread, where the
+    // warp-counting bar.sync behind __syncthreads() could complete early.
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cta_sync();
+    __syncwarp();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(pp.tmem, Cfg::TMEM_COLS);

@@ -80,7 +80,7 @@ __global__ void wait_selftest_kernel(unsigned int *status, unsigned long long ti
         abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    __syncthreads();
+    ptx::cta_sync();
     if (threadIdx.x == 0) {
         if (!ptx::mbar_wait_bounded(b, 0, timeout_ns, &abort_flag)) atomicOr(status, ST_TIMEOUT);
     }

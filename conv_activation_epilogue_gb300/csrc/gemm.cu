@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(192, 1)
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cta_sync();
     ptx::tc_fence_after();
     pp.tmem = misc[0];
 
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(192, 1)
             gemm_tile(t, p, mb, nb);
             const int n0 = nb * BN;
             uint32_t got = 1;
-            if (lane == 0) got = pipe_wait(pp, pp.tfull0 + 8 * acc, acc_phase) ? 1u : 0u;
+            if (lane == 0) got = epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase) ? 1u : 0u;
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) { ok = false; break; }
             ptx::tc_fence_after();
@@ -210,8 +210,13 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
     }
 
+    // Every role must be done before TMEM is released.  In the producer and
+    // MMA warps only lane 0 ran the role loop, so the warps arrive here
+    // diverged: the thread-counting barrier waits for every thread, where the
+    // warp-counting bar.sync behind __syncthreads() could complete early.
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cta_sync();
+    __syncwarp();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(pp.tmem, Cfg::TMEM_COLS);

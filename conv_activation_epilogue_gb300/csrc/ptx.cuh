@@ -14,6 +14,14 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Hardware fp32 tanh (MUFU), max relative error about 2^-11.
+__device__ __forceinline__ float tanh_approx(float x)
+{
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint64_t globaltimer()
 {
     uint64_t t;
@@ -43,6 +51,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// One poll of the barrier (the hardware may briefly suspend the thread).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t done;
@@ -56,16 +65,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// One poll with a suspend-time hint: a thread whose phase is not complete may
+// be parked for up to `suspend_ns`, which keeps long waits (the epilogue
+// waiting for a whole tile's main loop) off the issue slots the pipeline
+// roles need.  Not used on the latency-critical pipeline waits.
+__device__ __forceinline__ bool mbar_try_wait_sleepy(uint32_t bar, uint32_t parity, uint32_t suspend_ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return done != 0;
+}
+
 // Wait for the phase with parity `parity` of the barrier at `bar` to complete.
 // Bounded: gives up after `limit_ns` of %globaltimer time or 2^30 polls, or as
 // soon as `*abort` (if non-null) becomes non-zero.  Returns true on completion.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                                  const volatile uint32_t *abort)
+                                                  const volatile uint32_t *abort,
+                                                  uint32_t suspend_ns = 0)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (suspend_ns ? mbar_try_wait_sleepy(bar, parity, suspend_ns) : mbar_try_wait(bar, parity))
+            return true;
         if ((it & 31u) == 0) {
             if (abort != nullptr && *abort != 0u) return false;
             if (globaltimer() - t0 > limit_ns) return false;
@@ -139,6 +167,15 @@ __device__ __forceinline__ void bulk_wait()
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// CTA-wide barrier that counts threads, not warps (the non-.aligned form), so
+// it is correct even when the lanes of a warp reach it at different times --
+// as in the warp-specialised kernels, where one lane of a warp runs a role
+// loop while the other lanes wait.
+__device__ __forceinline__ void cta_sync()
+{
+    asm volatile("barrier.sync 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
