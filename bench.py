@@ -35,7 +35,7 @@ from conv_activation_epilogue_gb300 import synth  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "fused GEMM/conv+act TFLOP/s and % of GB300 dense bf16 tensor peak (1 GPU)"
-KERNEL_SOURCES = ["common.cuh", "ptx.cuh", "gemm.cu", "conv.cu", "conv_vec.cu", "elementwise.cu", "api.cu"]
+KERNEL_SOURCES = ["common.cuh", "ptx.cuh", "gemm.cu", "conv.cu", "conv_vec.cu", "conv_nhwc.cu", "elementwise.cu", "api.cu"]
 
 
 def env_int(name, default):
@@ -181,6 +181,24 @@ def workload_bytes(mmact, wl):
     Ho, Wo = mmact.mmact_conv2d_out_shape(wl.H, wl.W, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation)
     return (2.0 * (wl.N * wl.C * wl.H * wl.W + wl.Co * wl.C * wl.kh * wl.kw) + 4.0 * wl.Co +
             ob * wl.N * wl.Co * Ho * Wo)
+
+
+class NhwcProblem:
+    """A conv workload in channels-last layout (same values, transposed on the host)."""
+
+    def __init__(self, torch, mmact, wl, device, inputs=None):
+        self.mmact, self.wl = mmact, wl
+        inp = inputs if inputs is not None else wl.inputs()
+        self.x = codes_to(torch, np.ascontiguousarray(inp["x"].transpose(0, 2, 3, 1)), wl.dtype, device)
+        self.w = codes_to(torch, np.ascontiguousarray(inp["w"].transpose(0, 2, 3, 1)), wl.dtype, device)
+        self.bias = torch.from_numpy(inp["bias"]).to(device)
+        Ho, Wo = mmact.mmact_conv2d_out_shape(wl.H, wl.W, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation)
+        self.out = torch.empty((wl.N, Ho, Wo, wl.Co), dtype=torch_dtype(torch, wl.out_dtype), device=device)
+
+    def run(self, variant="fused", stream=None):
+        wl = self.wl
+        self.mmact.mmact_conv2d_nhwc(self.x, self.w, self.bias, self.out, wl.stride, wl.pads,
+                                     wl.dilation, wl.act, wl.alpha, stream)
 
 
 class Problem:
@@ -561,6 +579,15 @@ def sweep(torch, mmact, device, stream, peaks):
             rec[variant] = {"ms": round(ms, 5), "tflops": round(tf, 2),
                             "pct_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 2),
                             "alg_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+        if wl.kind == "conv":
+            # the same convolution on channels-last tensors (x NHWC, w [Co,kh,kw,C], y NHWC)
+            nprob = NhwcProblem(torch, mmact, wl, device, inputs=prob.host)
+            ms = time_graph(torch, lambda: nprob.run(), 20, stream)
+            tf = flops / (ms * 1e-3) / 1e12
+            rec["fused_nhwc"] = {"ms": round(ms, 5), "tflops": round(tf, 2),
+                                 "pct_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 2),
+                                 "alg_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+            del nprob
         st = mmact.mmact_get_last_error()
         rec["status"] = mmact.mmact_status_string(st)
         out[wl.name] = rec

@@ -56,7 +56,7 @@ mmact_status device_info(DeviceInfo **out)
         if (cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_status) != cudaSuccess)
             return MMACT_ERR_CUDA;
         if (setup_gemm_kernels() != cudaSuccess || setup_conv_kernels() != cudaSuccess ||
-            setup_conv_vec_kernels() != cudaSuccess)
+            setup_conv_vec_kernels() != cudaSuccess || setup_nhwc_kernels() != cudaSuccess)
             return MMACT_ERR_CUDA;
         if (g_encode == nullptr) {
             void *fn = nullptr;
@@ -90,15 +90,18 @@ CUtensorMapDataType tmap_type(mmact_dtype d)
 
 // Tiled map over a row-major tensor given innermost-first dims (elements) and
 // the byte strides of dims 1..rank-1, with a 128-byte swizzle (or none).
+// `estrides` (optional) are TMA traversal strides per dimension: a box of
+// box[i] elements along dimension i then delivers ceil(box[i] / estrides[i]).
 bool encode(CUtensorMap *m, mmact_dtype dt, int rank, const void *ptr, const uint64_t *dims,
-            const uint64_t *strides_bytes, const uint32_t *box, bool swizzle = true)
+            const uint64_t *strides_bytes, const uint32_t *box, bool swizzle = true,
+            const uint32_t *estrides = nullptr)
 {
     cuuint64_t gd[5], gs[4];
     cuuint32_t bx[5], es[5];
     for (int i = 0; i < rank; ++i) {
         gd[i] = dims[i];
         bx[i] = box[i];
-        es[i] = 1;
+        es[i] = estrides ? estrides[i] : 1;
     }
     for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
     CUresult r = g_encode(m, tmap_type(dt), (cuuint32_t)rank, const_cast<void *>(ptr), gd, gs, bx, es,
@@ -346,6 +349,95 @@ mmact_status conv_enqueue(const void *x, const void *w, const float *bias, void 
 
 int act_grid(const DeviceInfo *dev) { return dev->sm_count * 8; }
 
+mmact_status nhwc_enqueue(const void *x, const void *w, const float *bias, void *y, int64_t N,
+                          int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
+                          const int32_t *st, const int32_t *pd, const int32_t *dl, const ConvGeom &g,
+                          mmact_dtype in, mmact_dtype out, mmact_act act, float alpha,
+                          cudaStream_t stream)
+{
+    DeviceInfo *dev = nullptr;
+    mmact_status s = device_info(&dev);
+    if (s != MMACT_OK) return s;
+    const int64_t M = N * g.Ho * g.Wo;
+    if (M == 0 || Co == 0) return MMACT_OK;
+    if (C == 0) {
+        cudaError_t e = launch_bias_act(bias, y, M, Co, 0, Co, out_kind(out), (int)act, alpha, stream);
+        return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
+    }
+    NhwcLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    NhwcArgs &a = L.args;
+    a.Nb = (int)N;
+    a.C = (int)C;
+    a.H = (int)H;
+    a.W = (int)W;
+    a.Co = (int)Co;
+    a.kh = (int)kh;
+    a.kw = (int)kw;
+    a.sh = st[0];
+    a.sw = st[1];
+    a.pt = pd[0];
+    a.pl = pd[2];
+    a.dh = dl[0];
+    a.dw = dl[1];
+    a.Ho = (int)g.Ho;
+    a.Wo = (int)g.Wo;
+    a.M = (int)M;
+    a.ncb = (int)((C + 63) / 64);
+    // M tile: TH output rows x TW output columns of one image, 128 pixels
+    a.TW = g.Wo <= 32 ? 32 : 64;
+    if (a.TW * a.sw > 256) a.TW = 32;
+    a.TH = 128 / a.TW;
+    if (a.TW * a.sw > 256 || a.TH * a.sh > 256) return MMACT_ERR_UNSUPPORTED;
+    a.tiles_oh = (int)((g.Ho + a.TH - 1) / a.TH);
+    a.tiles_ow = (int)((g.Wo + a.TW - 1) / a.TW);
+    a.tiles_m = (int)(N * a.tiles_oh * a.tiles_ow);
+    // channels-last tiles come in widths 256, 128 and 64 (same cost model as the GEMM)
+    int bn = 256;
+    {
+        static const int widths[] = {256, 128, 64};
+        static const double rel_rate[] = {1.0, 0.61, 0.32};
+        double best = 1e300;
+        for (int i = 0; i < 3; ++i) {
+            const int64_t tiles = (int64_t)a.tiles_m * ((Co + widths[i] - 1) / widths[i]);
+            const double cost = (double)((tiles + dev->sm_count - 1) / dev->sm_count) * widths[i] / rel_rate[i];
+            if (cost < best * 0.999) {
+                best = cost;
+                bn = widths[i];
+            }
+        }
+    }
+    a.tiles_n = (int)((Co + bn - 1) / bn);
+    a.num_tiles = a.tiles_m * a.tiles_n;
+    a.num_kb = (int)(kh * kw) * a.ncb;
+    a.group_m = 16;
+    a.ab_bf16 = in == MMACT_BF16 ? 1 : 0;
+    a.act = (int)act;
+    a.alpha = alpha;
+    a.x = static_cast<const uint16_t *>(x);
+    a.bias = bias;
+    a.status = dev->status;
+    a.wait_ns = g_wait_ns.load();
+    L.tile_n = bn;
+    L.out = out_kind(out);
+    L.grid = (int)std::min<int64_t>(a.num_tiles, dev->sm_count);
+    const uint64_t dX[4] = {(uint64_t)C, (uint64_t)W, (uint64_t)H, (uint64_t)N};
+    const uint64_t sX[3] = {(uint64_t)C * 2, (uint64_t)W * C * 2, (uint64_t)H * W * C * 2};
+    const uint32_t bX[4] = {64, (uint32_t)(a.TW * a.sw), (uint32_t)(a.TH * a.sh), 1};
+    const uint32_t eX[4] = {1, (uint32_t)a.sw, (uint32_t)a.sh, 1};
+    const uint64_t dW[3] = {(uint64_t)C, (uint64_t)(kh * kw), (uint64_t)Co};
+    const uint64_t sW[2] = {(uint64_t)C * 2, (uint64_t)(kh * kw) * C * 2};
+    const uint32_t bW[3] = {64, 1, (uint32_t)bn};
+    const int e = elem_bytes(out);
+    const uint64_t dY[4] = {(uint64_t)Co, (uint64_t)g.Wo, (uint64_t)g.Ho, (uint64_t)N};
+    const uint64_t sY[3] = {(uint64_t)Co * e, (uint64_t)g.Wo * Co * e, (uint64_t)g.Ho * g.Wo * Co * e};
+    const uint32_t bY[4] = {(uint32_t)(128 / e), 32, 1, 1};
+    if (!encode(&L.tmX, in, 4, x, dX, sX, bX, true, eX) || !encode(&L.tmW, in, 3, w, dW, sW, bW) ||
+        !encode(&L.tmY, out, 4, y, dY, sY, bY))
+        return MMACT_ERR_CUDA;
+    return launch_conv_nhwc(L, stream) == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace mmact
 
@@ -422,6 +514,23 @@ MMACT_EXPORT mmact_status mmact_conv2d_split(const void *x, const void *w, const
                       act_grid(dev), st) == cudaSuccess
                ? MMACT_OK
                : MMACT_ERR_CUDA;
+}
+
+MMACT_EXPORT mmact_status mmact_conv2d_nhwc(const void *x, const void *w, const float *bias, void *y,
+                                            int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co,
+                                            int64_t kh, int64_t kw, const int32_t strides[2],
+                                            const int32_t pads[4], const int32_t dilations[2],
+                                            mmact_dtype in_dtype, mmact_dtype out_dtype,
+                                            mmact_act act, float alpha, void *stream)
+{
+    ConvGeom g;
+    mmact_status s = conv_check(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations,
+                                in_dtype, out_dtype, act, &g);
+    if (s != MMACT_OK) return s;
+    if (C % 8 != 0 || Co % 8 != 0) return MMACT_ERR_UNSUPPORTED;
+    if (N * g.Ho * g.Wo > MAX_DIM) return MMACT_ERR_UNSUPPORTED;
+    return nhwc_enqueue(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations, g, in_dtype,
+                        out_dtype, act, alpha, static_cast<cudaStream_t>(stream));
 }
 
 MMACT_EXPORT mmact_status mmact_conv2d_out_shape(int64_t H, int64_t W, int64_t kh, int64_t kw,

@@ -112,11 +112,22 @@ struct TileN {
     static constexpr uint32_t TMEM_COLS = 2u * ACC_STRIDE;
 };
 
-template <int BN, int STAGES>
+//
+// B_KMAJOR: the B stage is instead [BN rows x 64 K] K-major with the same
+// 128-byte swizzle as A (rows are output columns; used when B is given as
+// [N, K] with K contiguous, e.g. a channels-last filter).
+//
+// THREAD_FILLED: some operand stage bytes were written by ordinary shared
+// stores of producer threads (the conv gathers) rather than by TMA.  Those
+// threads only store and arrive on the full barrier (release); this thread,
+// after acquiring the barrier, issues the one generic-to-async proxy fence
+// that makes the stores visible to the tensor core's operand reads.
+template <int BN, int STAGES, bool B_KMAJOR = false, bool THREAD_FILLED = false>
 __device__ void mma_role(const Pipe &pp, uint32_t sA, uint32_t sB, int num_tiles, int num_kb,
                          uint32_t idesc)
 {
-    constexpr uint32_t A_BYTES = 128 * 64 * 2, B_BYTES = TileN<BN>::B_BYTES;
+    constexpr uint32_t A_BYTES = 128 * 64 * 2;
+    constexpr uint32_t B_BYTES = B_KMAJOR ? (uint32_t)BN * 128u : TileN<BN>::B_BYTES;
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -125,12 +136,14 @@ __device__ void mma_role(const Pipe &pp, uint32_t sA, uint32_t sB, int num_tiles
         const uint32_t d = pp.tmem + acc * TileN<BN>::ACC_STRIDE;
         for (int kb = 0; kb < num_kb; ++kb) {
             if (!pipe_wait(pp, pp.full0 + 8 * stage, phase)) { ok = false; break; }
+            if constexpr (THREAD_FILLED) ptx::fence_proxy_async_smem();
             ptx::tc_fence_after();
             const uint32_t a0 = sA + stage * A_BYTES, b0 = sB + stage * B_BYTES;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const uint64_t ad = ptx::smem_desc(a0 + 32u * k, 16u, 1024u, ptx::SWIZZLE_128B);
-                const uint64_t bd = ptx::smem_desc(b0 + 2048u * k, 8192u, 1024u, ptx::SWIZZLE_128B);
+                const uint64_t bd = B_KMAJOR ? ptx::smem_desc(b0 + 32u * k, 16u, 1024u, ptx::SWIZZLE_128B)
+                                             : ptx::smem_desc(b0 + 2048u * k, 8192u, 1024u, ptx::SWIZZLE_128B);
                 ptx::mma_f16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
             ptx::mma_commit(pp.empty0 + 8 * stage);
@@ -169,9 +182,22 @@ __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, 
     ptx::tmem_ld32(taddr, r0);
     if constexpr (WIDE) ptx::tmem_ld32(taddr + 32, r1);
     float bc[COLS];
+    if (!BIAS_ROW && bias_col != nullptr && nvalid >= COLS &&
+        (reinterpret_cast<uintptr_t>(bias_col) & 15u) == 0) {
+        // the whole segment is in range and 16-byte aligned: vector loads
 #pragma unroll
-    for (int j = 0; j < COLS; ++j)
-        bc[j] = BIAS_ROW ? brow : ((bias_col != nullptr && j < nvalid) ? __ldg(bias_col + j) : 0.0f);
+        for (int j = 0; j < COLS; j += 4) {
+            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(bias_col + j));
+            bc[j] = b4.x;
+            bc[j + 1] = b4.y;
+            bc[j + 2] = b4.z;
+            bc[j + 3] = b4.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < COLS; ++j)
+            bc[j] = BIAS_ROW ? brow : ((bias_col != nullptr && j < nvalid) ? __ldg(bias_col + j) : 0.0f);
+    }
     ptx::tmem_ld_wait(r0);
     if constexpr (WIDE) ptx::tmem_ld_wait(r1);
     if constexpr (OUT != OUT_F32 && !WIDE) {

@@ -148,8 +148,8 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0)
-            mma_role<BN, STAGES>(pp, sA, sB, p.num_tiles, p.num_kb,
-                                 ptx::idesc_f16(p.ab_bf16 != 0, false, true, 128, BN));
+            mma_role<BN, STAGES, false, true>(pp, sA, sB, p.num_tiles, p.num_kb,
+                                              ptx::idesc_f16(p.ab_bf16 != 0, false, true, 128, BN));
     } else if (warp >= 6) {
         // ---------------------------------------------------- B-tile gather --
         // Thread j owns pixel column j of every B tile.  For each stage it
@@ -204,8 +204,7 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
                         ptx::st_shared_u16(at + a_tile_offset(j, kl), v);
                     }
                 }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
+                __syncwarp();   // the MMA thread fences the stores into the async proxy
                 if (lane == 0) ptx::mbar_arrive(pp.full0 + 8 * stage);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }

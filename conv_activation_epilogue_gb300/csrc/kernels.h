@@ -63,6 +63,37 @@ cudaError_t setup_gemm_kernels();
 cudaError_t setup_conv_kernels();
 cudaError_t setup_conv_vec_kernels();
 cudaError_t launch_conv_vec(const ConvLaunch &L, cudaStream_t stream);
+// Channels-last conv2d as implicit GEMM: M = output pixels (n, oh, ow),
+// N = output channels, K = (r, q, ci).
+struct NhwcArgs {
+    int Nb, C, H, W, Co, kh, kw;
+    int sh, sw, pt, pl, dh, dw;
+    int Ho, Wo;
+    int M;               // Nb * Ho * Wo output pixels
+    int ncb;             // channel blocks of 64 per tap
+    int TW, TH;          // output pixels per tile: TH rows x TW columns (TW * TH = 128)
+    int tiles_oh, tiles_ow;
+    int tiles_m, tiles_n, num_tiles, num_kb;   // tiles_m = Nb * tiles_oh * tiles_ow; num_kb = kh * kw * ncb
+    int group_m;
+    int ab_bf16;
+    int act;
+    float alpha;
+    const uint16_t *x;
+    const float *bias;   // [Co] or null
+    unsigned int *status;
+    unsigned long long wait_ns;
+};
+
+struct NhwcLaunch {
+    CUtensorMap tmX, tmW, tmY;   // x as {C, W, H, N}; filter as {C, kh*kw, Co}; y as {Co, Wo, Ho, N}
+    NhwcArgs args;
+    int tile_n;
+    int out;
+    int grid;
+};
+
+cudaError_t setup_nhwc_kernels();
+cudaError_t launch_conv_nhwc(const NhwcLaunch &L, cudaStream_t stream);
 cudaError_t launch_gemm(const GemmLaunch &L, cudaStream_t stream);
 cudaError_t launch_conv(const ConvLaunch &L, cudaStream_t stream);
 // out[i] = act(ws[i]) for i < count (ws fp32, out of dtype `out`).

@@ -26,6 +26,7 @@ _lib = None
 # Exported C symbols, as declared in include/mmact.h.
 SYMBOLS = [
     "mmact_gemm", "mmact_gemm_split", "mmact_gemm_split_noalloc", "mmact_conv2d", "mmact_conv2d_split",
+    "mmact_conv2d_nhwc",
     "mmact_conv2d_out_shape", "mmact_get_last_error", "mmact_set_wait_timeout_ns",
     "mmact_selftest_wait_timeout", "mmact_set_gemm_tile_n", "mmact_status_string", "mmact_version",
 ]
@@ -57,6 +58,8 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     conv = [vp, vp, vp, vp] + [i64] * 7 + [p_i32, p_i32, p_i32, ci, ci, ci, f32]
     L.mmact_conv2d.argtypes = conv + [vp]
     L.mmact_conv2d_split.argtypes = conv + [vp, vp]
+    L.mmact_conv2d_nhwc.argtypes = conv + [vp]
+    L.mmact_conv2d_nhwc.restype = ci
     L.mmact_conv2d_out_shape.argtypes = [i64, i64, i64, i64, p_i32, p_i32, p_i32,
                                          ctypes.POINTER(i64), ctypes.POINTER(i64)]
     L.mmact_get_last_error.argtypes = [vp]
@@ -214,6 +217,28 @@ def mmact_conv2d_split(x, w, bias, y, workspace, stride=(1, 1), pads=(0, 0, 0, 0
         raise ValueError("workspace must hold y.numel() fp32 elements")
     _check(L.mmact_conv2d_split(*args, DTYPE[x.dtype], DTYPE[y.dtype], ACT[act], float(alpha), pws,
                                 _stream_handle(stream)), "mmact_conv2d_split")
+
+
+def mmact_conv2d_nhwc(x, w, bias, y, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1),
+                      act: str = "tanh", alpha: float = 0.0, stream=None) -> None:
+    """Channels-last y = act(conv2d(x, w) + bias): x [N,H,W,C], w [Co,kh,kw,C], y [N,Ho,Wo,Co]."""
+    L = load()
+    px = _dev(x, "x", _IN)
+    pw = _dev(w, "w", _IN)
+    py = _dev(y, "y", _OUT)
+    if x.dim() != 4 or w.dim() != 4 or y.dim() != 4:
+        raise ValueError("x, w, y must be 4-D (NHWC / [Co,kh,kw,C] / NHWC)")
+    N, H, W, C = x.shape
+    Co, kh, kw, C2 = w.shape
+    if C2 != C or w.dtype != x.dtype:
+        raise ValueError("w must be [Co, kh, kw, C] with x's dtype")
+    Ho, Wo = mmact_conv2d_out_shape(H, W, kh, kw, stride, pads, dilation)
+    if tuple(y.shape) != (N, Ho, Wo, Co):
+        raise ValueError(f"y must be {(N, Ho, Wo, Co)}")
+    _check(L.mmact_conv2d_nhwc(px, pw, _bias_ptr(bias, Co), py, N, C, H, W, Co, kh, kw,
+                               _i32(stride, 2), _i32(pads, 4), _i32(dilation, 2), DTYPE[x.dtype],
+                               DTYPE[y.dtype], ACT[act], float(alpha), _stream_handle(stream)),
+           "mmact_conv2d_nhwc")
 
 
 def mmact_get_last_error(stream=None) -> int:

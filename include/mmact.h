@@ -180,6 +180,27 @@ mmact_status mmact_gemm_split_noalloc(const void *A, const void *B, const float 
                                       mmact_act act, float alpha, void *stream);
 
 /*
+ * Channels-last fused conv2d + bias + activation (the layout-converting
+ * member of the fused_matmul_relu article's fusion families applied to the
+ * Fused ConvTanh operator):  y = act(conv2d(x, w) + bias).
+ *   x    [N, H, W, C] in_dtype (F16 or BF16), channels innermost (NHWC)
+ *   w    [Co, kh, kw, C] in_dtype, channels innermost
+ *   bias [Co] fp32, or NULL
+ *   y    [N, Ho, Wo, Co] out_dtype (F32, F16 or BF16), NHWC; fully overwritten
+ * strides / pads / dilations and Ho, Wo as for mmact_conv2d.  Requires
+ * C % 8 == 0 and Co % 8 == 0 (16-byte channel vectors and rows), else
+ * MMACT_ERR_UNSUPPORTED.  N == 0 or Co == 0 enqueues nothing; C == 0 gives
+ * y = act(bias).
+ */
+mmact_status mmact_conv2d_nhwc(const void *x, const void *w, const float *bias, void *y,
+                               int64_t N, int64_t C, int64_t H, int64_t W,
+                               int64_t Co, int64_t kh, int64_t kw,
+                               const int32_t strides[2], const int32_t pads[4],
+                               const int32_t dilations[2],
+                               mmact_dtype in_dtype, mmact_dtype out_dtype,
+                               mmact_act act, float alpha, void *stream);
+
+/*
  * Output spatial size of a conv geometry (host only, no CUDA call).  Writes
  * Ho and Wo (host pointers) and returns MMACT_OK, or MMACT_ERR_INVALID_ARG for
  * a bad geometry (non-positive kernel/stride/dilation, negative pad or size,
