@@ -250,24 +250,15 @@ mmact_status conv_check(const void *x, const void *w, const float *bias, const v
     return MMACT_OK;
 }
 
-mmact_status conv_enqueue(const void *x, const void *w, const float *bias, void *y, int64_t N,
-                          int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
-                          const int32_t *st, const int32_t *pd, const int32_t *dl, const ConvGeom &g,
-                          mmact_dtype in, mmact_dtype out, mmact_act act, float alpha,
-                          cudaStream_t stream)
+// Host-side plan of a conv launch: the GEMM view, the producer (general
+// gather, vectorised global-load gather, or vectorised window), the tile
+// shape and the window box.  No device work.
+void conv_plan(int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
+               const int32_t *st, const int32_t *pd, const int32_t *dl, const ConvGeom &g,
+               mmact_dtype in, mmact_dtype out, ConvArgs &a)
 {
-    DeviceInfo *dev = nullptr;
-    mmact_status s = device_info(&dev);
-    if (s != MMACT_OK) return s;
     const int64_t P = g.Ho * g.Wo;
-    if (N == 0 || Co == 0 || P == 0) return MMACT_OK;
-    if (C == 0) {
-        cudaError_t e = launch_bias_act(bias, y, N * Co, P, 1, Co, out_kind(out), (int)act, alpha, stream);
-        return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
-    }
-    ConvLaunch L;
-    std::memset(&L, 0, sizeof(L));
-    ConvArgs &a = L.args;
+    std::memset(&a, 0, sizeof(a));
     a.Nb = (int)N;
     a.C = (int)C;
     a.H = (int)H;
@@ -290,15 +281,7 @@ mmact_status conv_enqueue(const void *x, const void *w, const float *bias, void 
     a.num_tiles = (int)(N * a.tiles_co * a.tiles_p);
     a.num_kb = (a.K + 63) / 64;
     a.ab_bf16 = in == MMACT_BF16 ? 1 : 0;
-    a.act = (int)act;
-    a.alpha = alpha;
     a.out_elem_bytes = elem_bytes(out);
-    a.x = static_cast<const uint16_t *>(x);
-    a.w = static_cast<const uint16_t *>(w);
-    a.bias = bias;
-    a.y = y;
-    a.status = dev->status;
-    a.wait_ns = g_wait_ns.load();
     a.a_tma = (a.K % 8 == 0) ? 1 : 0;
     a.y_tma = ((P * a.out_elem_bytes) % 16 == 0) ? 1 : 0;
     // Vectorised producer: whole 16-byte input chunks per row (W % 8 == 0),
@@ -318,13 +301,72 @@ mmact_status conv_enqueue(const void *x, const void *w, const float *bias, void 
             a.TH = 4;
         }
     }
-    if (a.vec) {
-        a.tiles_oh = (int)((g.Ho + a.TH - 1) / a.TH);
-        a.tiles_ow = (int)((g.Wo + a.TW - 1) / a.TW);
-        a.num_tiles = (int)(N * a.tiles_oh * a.tiles_ow * a.tiles_co);
+    if (!a.vec) return;
+    a.tiles_oh = (int)((g.Ho + a.TH - 1) / a.TH);
+    a.tiles_ow = (int)((g.Wo + a.TW - 1) / a.TW);
+    a.num_tiles = (int)(N * a.tiles_oh * a.tiles_ow * a.tiles_co);
+    // Input window per 64-row K block (conv_vec.cu, WIN): the channels 64
+    // consecutive rows (ci, r, q) can span; the rows of every tap r (a row
+    // stride of sh when dh is a multiple of sh); an 8-aligned column span wide
+    // enough for every lane's chunk loads at every q.
+    const int64_t taps = kh * kw;
+    const int S = a.sw, nch = S == 1 ? 2 : 3, vpr = a.TW / 8;
+    const int64_t CB = std::min<int64_t>(C, (62 + taps) / taps + 1);
+    const bool hstride = a.sh > 1 && a.sh <= 8 && (kh == 1 || a.dh % a.sh == 0);
+    const int64_t esh = hstride ? a.sh : 1;
+    const int64_t HB = hstride ? a.TH + (kh - 1) * (a.dh / a.sh)
+                               : (int64_t)(a.TH - 1) * a.sh + (kh - 1) * a.dh + 1;
+    const int64_t c0max = ((int64_t)(vpr - 1) * 8 * S + 7 + (kw - 1) * a.dw) >> 3;
+    const int64_t WB = 8 * (c0max + nch);
+    const int64_t raw = WB * HB * CB * 2;
+    if (raw <= CONV_WIN_MAX_BYTES && WB <= 256 && HB * esh <= 256 && CB <= 256) {
+        a.win = 1;
+        a.WB = (int)WB;
+        a.HB = (int)HB;
+        a.CB = (int)CB;
+        a.rstep = hstride ? a.dh / a.sh : a.dh;
+        a.rowmul = hstride ? 1 : a.sh;
+        a.raw_bytes = (int)raw;
     }
+}
+
+mmact_status conv_enqueue(const void *x, const void *w, const float *bias, void *y, int64_t N,
+                          int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
+                          const int32_t *st, const int32_t *pd, const int32_t *dl, const ConvGeom &g,
+                          mmact_dtype in, mmact_dtype out, mmact_act act, float alpha,
+                          cudaStream_t stream)
+{
+    DeviceInfo *dev = nullptr;
+    mmact_status s = device_info(&dev);
+    if (s != MMACT_OK) return s;
+    const int64_t P = g.Ho * g.Wo;
+    if (N == 0 || Co == 0 || P == 0) return MMACT_OK;
+    if (C == 0) {
+        cudaError_t e = launch_bias_act(bias, y, N * Co, P, 1, Co, out_kind(out), (int)act, alpha, stream);
+        return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
+    }
+    ConvLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    ConvArgs &a = L.args;
+    conv_plan(N, C, H, W, Co, kh, kw, st, pd, dl, g, in, out, a);
+    a.act = (int)act;
+    a.alpha = alpha;
+    a.x = static_cast<const uint16_t *>(x);
+    a.w = static_cast<const uint16_t *>(w);
+    a.bias = bias;
+    a.y = y;
+    a.status = dev->status;
+    a.wait_ns = g_wait_ns.load();
     L.out = out_kind(out);
     L.grid = (int)std::min<int64_t>(a.num_tiles, dev->sm_count);
+    if (a.win) {
+        const uint32_t esh = (uint32_t)(a.rowmul == 1 && a.sh > 1 ? a.sh : 1);
+        const uint64_t d[4] = {(uint64_t)W, (uint64_t)H, (uint64_t)C, (uint64_t)N};
+        const uint64_t sb[3] = {(uint64_t)W * 2, (uint64_t)H * W * 2, (uint64_t)C * H * W * 2};
+        const uint32_t bx[4] = {(uint32_t)a.WB, (uint32_t)a.HB * esh, (uint32_t)a.CB, 1};
+        const uint32_t es[4] = {1, esh, 1, 1};
+        if (!encode(&L.tmX, in, 4, x, d, sb, bx, false, es)) return MMACT_ERR_CUDA;
+    }
     if (a.vec && a.TW == 64) {
         const int e = a.out_elem_bytes;
         const uint64_t d[4] = {(uint64_t)g.Wo, (uint64_t)g.Ho, (uint64_t)Co, (uint64_t)N};
@@ -545,6 +587,20 @@ MMACT_EXPORT mmact_status mmact_conv2d_out_shape(int64_t H, int64_t W, int64_t k
     *Ho = g.Ho;
     *Wo = g.Wo;
     return MMACT_OK;
+}
+
+MMACT_EXPORT int mmact_conv2d_producer(int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co,
+                                       int64_t kh, int64_t kw, const int32_t strides[2],
+                                       const int32_t pads[4], const int32_t dilations[2],
+                                       mmact_dtype in_dtype, mmact_dtype out_dtype)
+{
+    ConvGeom g;
+    if (N < 0 || C <= 0 || Co < 0 || !valid_in(in_dtype) || !valid_out(out_dtype)) return -1;
+    if (conv_geom(H, W, kh, kw, strides, pads, dilations, &g) != MMACT_OK) return -1;
+    if (C * H * W > MAX_DIM || Co * g.Ho * g.Wo > MAX_DIM || C * kh * kw > MAX_DIM) return -1;
+    ConvArgs a;
+    conv_plan(N, C, H, W, Co, kh, kw, strides, pads, dilations, g, in_dtype, out_dtype, a);
+    return a.win ? MMACT_CONV_WINDOW : a.vec ? MMACT_CONV_VECTOR : MMACT_CONV_GATHER;
 }
 
 MMACT_EXPORT mmact_status mmact_get_last_error(void *stream)

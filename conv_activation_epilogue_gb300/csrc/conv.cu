@@ -187,10 +187,7 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
                         if (++r == p.kh) { r = 0; cbase += HW; }
                     }
                 }
-                uint32_t go = 1;
-                if (lane == 0) go = pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u) ? 1u : 0u;
-                go = __shfl_sync(0xffffffffu, go, 0);
-                if (!go) { ok = false; break; }
+                if (!warp_pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u)) { ok = false; break; }
                 const uint32_t bt = sB + stage * Cfg::B_BYTES;
 #pragma unroll
                 for (int kl = 0; kl < 64; ++kl) ptx::st_shared_u16(bt + b_tile_offset(kl, j), vals[kl]);
@@ -223,10 +220,7 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
             const int co_row0 = cb * 128 + qd * 32;
             const int co = co_row0 + lane;
             const float brow = (p.bias != nullptr && co < p.Co) ? __ldg(p.bias + co) : 0.0f;
-            uint32_t got = 1;
-            if (lane == 0) got = epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase) ? 1u : 0u;
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (!got) { ok = false; break; }
+            if (!warp_epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t tbase = pp.tmem + ((uint32_t)(qd * 32) << 16) + acc * BN;
 #pragma unroll 1

@@ -171,10 +171,7 @@ __global__ void __launch_bounds__(NhwcCfg<BN>::THREADS, 1)
             const int n0 = nb * BN;
             const int oh = toh * p.TH + (qd * 32) / p.TW;
             const int ow = tow * p.TW + (qd * 32) % p.TW;
-            uint32_t got = 1;
-            if (lane == 0) got = epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase) ? 1u : 0u;
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (!got) { ok = false; break; }
+            if (!warp_epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t tbase = pp.tmem + ((uint32_t)(qd * 32) << 16) + acc * TileN<BN>::ACC_STRIDE;
 #pragma unroll 1

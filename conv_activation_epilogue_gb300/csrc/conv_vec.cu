@@ -21,23 +21,40 @@
 // for every lane of the warp, so the selection is a warp-uniform switch.  The
 // vector is stored with one 16-byte shared store into the 128-byte swizzled
 // MN-major tile that tcgen05.mma reads.
+//
+// Window variant (WIN).  Read straight from global memory, every input
+// element is fetched once per filter tap that touches it (9 times for a 3x3
+// filter), and those redundant 16-byte loads are what limits the producer.
+// With WIN the TMA warp also loads, per 64-row K block, the raw input window
+// the block needs -- the <= CB channels its rows (ci, r, q) span, every input
+// row the tile's output rows read for any r, and an 8-aligned column span
+// covering every q -- as one 4-D box of x {W, H, C, N} into shared memory
+// (zero fill outside the image is the padding; a row traversal stride of sh
+// skips the rows no tap reads when dh is a multiple of sh).  The gather
+// warps then build the B tile from that window with 16-byte shared loads and
+// the same byte picks, so global memory sees each input element about once
+// per tile and channel block.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace mmact {
 
+template <bool WIN>
 struct ConvVecCfg {
     static constexpr int BM = 128, BN = 256, BK = 64;
     static constexpr int A_BYTES = BM * BK * 2;          // 16 KB
     static constexpr int B_BYTES = BK * BN * 2;          // 32 KB (4 chunks of 64 pixels)
-    static constexpr int STAGES = 4;
+    static constexpr int STAGES = WIN ? 3 : 4;
+    static constexpr int RSTAGES = WIN ? 2 : 0;          // input-window ring
+    static constexpr int RAW_MAX = CONV_WIN_MAX_BYTES;   // bytes of one window slot
     static constexpr int EPI_BYTES = 4 * 2 * 4096;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-    static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_RAW = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_EPI = OFF_RAW + RSTAGES * RAW_MAX;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * RSTAGES;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int GATHER_WARPS = 8;
@@ -89,12 +106,13 @@ __device__ __forceinline__ void pick8(int sh, const uint32_t *w, uint32_t (&o)[4
     }
 }
 
-template <int OUT, int S>
-__global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
+template <int OUT, int S, bool WIN>
+__global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
     conv_vec_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmY,
-                    const __grid_constant__ CUtensorMap tmY4, const ConvArgs p)
+                    const __grid_constant__ CUtensorMap tmY4, const __grid_constant__ CUtensorMap tmX,
+                    const ConvArgs p)
 {
-    using Cfg = ConvVecCfg;
+    using Cfg = ConvVecCfg<WIN>;
     constexpr int STAGES = Cfg::STAGES, BN = Cfg::BN;
     constexpr int COLS = OUT == OUT_F32 ? 32 : 64;
     constexpr int NCH = S == 1 ? 2 : 3;                 // aligned chunks per output vector
@@ -116,11 +134,17 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
     pp.abort = misc + 1;
     pp.status = p.status;
     pp.wait_ns = p.wait_ns;
+    const uint32_t rfull0 = pp.drain + 8;                // input-window ring (WIN)
+    const uint32_t rempty0 = rfull0 + 8 * Cfg::RSTAGES;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(pp.full0 + 8 * s, Cfg::GATHER_WARPS + 1);   // gather warps + filter TMA
             ptx::mbar_init(pp.empty0 + 8 * s, 1);
+        }
+        for (int s = 0; s < Cfg::RSTAGES; ++s) {
+            ptx::mbar_init(rfull0 + 8 * s, 1);                         // window TMA
+            ptx::mbar_init(rempty0 + 8 * s, Cfg::GATHER_WARPS);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(pp.tfull0 + 8 * a, 1);
@@ -145,11 +169,16 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
         if (lane == 0) {
             // ---------------------------------------------- filter producer --
             ptx::prefetch_tensormap(&tmW);
+            if constexpr (WIN) ptx::prefetch_tensormap(&tmX);
+            const int taps = p.kh * p.kw;
             uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;
+            uint32_t rst = 0, rph = 0, rissued = 0, rlast = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
                 int n, toh, tow, cb;
                 vconv_tile(t, p, n, toh, tow, cb);
+                const int y0 = toh * p.TH * p.sh - p.pt;                  // window origin (WIN)
+                const int x0 = (tow * p.TW * S - p.pl) & ~7;              // 8-aligned: TMA x rule
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u)) { ok = false; break; }
                     const uint32_t fb = pp.full0 + 8 * stage;
@@ -158,17 +187,119 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    if constexpr (WIN) {
+                        if (!pipe_wait(pp, rempty0 + 8 * rst, rph ^ 1u)) { ok = false; break; }
+                        const uint32_t rb = rfull0 + 8 * rst;
+                        ptx::mbar_arrive_expect_tx(rb, (uint32_t)p.raw_bytes);
+                        ptx::tma_load_4d(base + Cfg::OFF_RAW + rst * Cfg::RAW_MAX, &tmX, rb, x0, y0,
+                                         (kb * 64) / taps, n);
+                        rissued |= 1u << rst;
+                        rlast = (rlast & ~(1u << rst)) | (rph << rst);
+                        if (++rst == (uint32_t)Cfg::RSTAGES) { rst = 0; rph ^= 1u; }
+                    }
                 }
             }
             if (!ok) pipe_fail(pp);
             for (int s = 0; s < STAGES; ++s)
                 if (issued & (1u << s))
                     ptx::mbar_wait_bounded(pp.full0 + 8 * s, (last_par >> s) & 1u, DRAIN_NS, nullptr);
+            for (int s = 0; s < Cfg::RSTAGES; ++s)
+                if (rissued & (1u << s))
+                    ptx::mbar_wait_bounded(rfull0 + 8 * s, (rlast >> s) & 1u, DRAIN_NS, nullptr);
         }
     } else if (warp == 1) {
         if (lane == 0)
             mma_role<BN, STAGES, false, true>(pp, sA, sB, p.num_tiles, p.num_kb,
                                               ptx::idesc_f16(p.ab_bf16 != 0, false, true, 128, BN));
+    } else if (warp >= 6 && WIN) {
+        // ------------------------------------ B-tile build from the window --
+        // Same lane -> (tile row, 8-pixel vector) mapping and B-tile
+        // addressing as the global-load gather below.  Window element
+        // (cc, hr, wc) is x[n][c_lo + cc][y0 + hr*esh][x0 + wc]; row k =
+        // (ci, r, q) of output pixel (t_row, 8 t_vec + e) reads window row
+        // (ci - c_lo, t_row*rowmul + r*rstep) at column u + 8 S t_vec + S e
+        // with u = (tile column origin - x0) + q*dw.
+        constexpr int ROWS = 64 / Cfg::GATHER_WARPS;
+        constexpr int GRP = S == 1 ? 8 : 4;
+        static_assert(ROWS % GRP == 0, "row split");
+        const int gw = warp - 6;
+        const int taps = p.kh * p.kw;
+        const int vpr = p.TW >> 3;
+        const int t_row = lane / vpr, t_vec = lane - (lane / vpr) * vpr;
+        const int pcol = t_row * p.TW + t_vec * 8;
+        const uint32_t lane_off = (uint32_t)((pcol >> 6) * 8192);
+        const uint32_t pc8 = (uint32_t)((pcol >> 3) & 7);
+        const int lane_raw = t_row * p.rowmul * p.WB + t_vec * 8 * S;
+        uint32_t stage = 0, phase = 0, rst = 0, rph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+            int n, toh, tow, cb;
+            vconv_tile(t, p, n, toh, tow, cb);
+            const int xs = tow * p.TW * S - p.pl;
+            const int off0 = xs - (xs & ~7);
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                // lanes 0..ROWS-1 decode this warp's rows before the waits
+                int my_row = 0, my_u = 0, my_ok = 0;
+                if (lane < ROWS) {
+                    const int k = kb * 64 + gw * ROWS + lane;
+                    if (k < p.K) {
+                        const int ci = k / taps;
+                        const int tap = k - ci * taps;
+                        const int r = tap / p.kw;
+                        my_row = ((ci - (kb * 64) / taps) * p.HB + r * p.rstep) * p.WB;
+                        my_u = off0 + (tap - r * p.kw) * p.dw;
+                        my_ok = 1;
+                    }
+                }
+                if (!warp_pipe_wait(pp, rfull0 + 8 * rst, rph) ||
+                    !warp_pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t rbuf = base + Cfg::OFF_RAW + rst * Cfg::RAW_MAX + 2u * (uint32_t)lane_raw;
+                const uint32_t bt = sB + stage * Cfg::B_BYTES + lane_off;
+#pragma unroll
+                for (int g = 0; g < ROWS; g += GRP) {
+                    uint4 ch[GRP][NCH];
+                    int shift[GRP], rok[GRP];
+#pragma unroll
+                    for (int i = 0; i < GRP; ++i) {
+                        const int row = __shfl_sync(0xffffffffu, my_row, g + i);
+                        const int u = __shfl_sync(0xffffffffu, my_u, g + i);
+                        rok[i] = __shfl_sync(0xffffffffu, my_ok, g + i);
+                        shift[i] = u & 7;
+                        const uint32_t a = rbuf + 2u * (uint32_t)(row + (u & ~7));
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) ch[i][c] = ptx::ld_shared_v4(a + 16u * c);
+                    }
+#pragma unroll
+                    for (int i = 0; i < GRP; ++i) {
+                        uint32_t w[4 * NCH];
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) {
+                            w[4 * c + 0] = ch[i][c].x;
+                            w[4 * c + 1] = ch[i][c].y;
+                            w[4 * c + 2] = ch[i][c].z;
+                            w[4 * c + 3] = ch[i][c].w;
+                        }
+                        uint32_t o[4];
+                        pick8<S>(shift[i], w, o);
+                        if (!rok[i]) o[0] = o[1] = o[2] = o[3] = 0u;   // rows past K
+                        const int kl = gw * ROWS + g + i;
+                        ptx::st_shared_v4(bt + (uint32_t)kl * 128u + ((pc8 ^ (uint32_t)(kl & 7)) << 4), o[0],
+                                          o[1], o[2], o[3]);
+                    }
+                }
+                __syncwarp();   // the MMA thread fences the stores into the async proxy
+                if (lane == 0) {
+                    ptx::mbar_arrive(rempty0 + 8 * rst);
+                    ptx::mbar_arrive(pp.full0 + 8 * stage);
+                }
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                if (++rst == (uint32_t)Cfg::RSTAGES) { rst = 0; rph ^= 1u; }
+            }
+        }
+        if (!ok) pipe_fail(pp);
     } else if (warp >= 6) {
         // ---------------------------------------------------- B-tile gather --
         // Rows are handled in groups of 4: the loads of a whole group are
@@ -234,10 +365,7 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
                         }
                     }
                     if (g == 0) {
-                        uint32_t go = 1;
-                        if (lane == 0) go = pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u) ? 1u : 0u;
-                        go = __shfl_sync(0xffffffffu, go, 0);
-                        if (!go) { ok = false; break; }
+                        if (!warp_pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u)) { ok = false; break; }
                     }
 #pragma unroll
                     for (int i = 0; i < GRP; ++i) {
@@ -275,10 +403,7 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
             const int co_row0 = cb * 128 + qd * 32;
             const int co = co_row0 + lane;
             const float brow = (p.bias != nullptr && co < p.Co) ? __ldg(p.bias + co) : 0.0f;
-            uint32_t got = 1;
-            if (lane == 0) got = epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase) ? 1u : 0u;
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (!got) { ok = false; break; }
+            if (!warp_epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t tbase = pp.tmem + ((uint32_t)(qd * 32) << 16) + acc * BN;
 #pragma unroll 1
@@ -332,45 +457,60 @@ __global__ void __launch_bounds__(ConvVecCfg::THREADS, 1)
     }
 }
 
-template <int OUT, int S>
+template <int OUT, int S, bool WIN>
 static cudaError_t launch_vec_t(const ConvLaunch &L, cudaStream_t stream)
 {
-    conv_vec_kernel<OUT, S><<<L.grid, ConvVecCfg::THREADS, ConvVecCfg::SMEM_BYTES, stream>>>(
-        L.tmW, L.tmY, L.tmY4, L.args);
+    using Cfg = ConvVecCfg<WIN>;
+    conv_vec_kernel<OUT, S, WIN><<<L.grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(L.tmW, L.tmY, L.tmY4,
+                                                                                      L.tmX, L.args);
     return cudaGetLastError();
 }
 
-template <int OUT, int S>
+template <int OUT, int S, bool WIN>
 static cudaError_t setup_vec_t()
 {
-    return cudaFuncSetAttribute(conv_vec_kernel<OUT, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                ConvVecCfg::SMEM_BYTES);
+    return cudaFuncSetAttribute(conv_vec_kernel<OUT, S, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                ConvVecCfg<WIN>::SMEM_BYTES);
+}
+
+template <bool WIN>
+static cudaError_t setup_vec_w()
+{
+    cudaError_t e = setup_vec_t<OUT_BF16, 1, WIN>();
+    if (e == cudaSuccess) e = setup_vec_t<OUT_F16, 1, WIN>();
+    if (e == cudaSuccess) e = setup_vec_t<OUT_F32, 1, WIN>();
+    if (e == cudaSuccess) e = setup_vec_t<OUT_BF16, 2, WIN>();
+    if (e == cudaSuccess) e = setup_vec_t<OUT_F16, 2, WIN>();
+    if (e == cudaSuccess) e = setup_vec_t<OUT_F32, 2, WIN>();
+    return e;
 }
 
 cudaError_t setup_conv_vec_kernels()
 {
-    cudaError_t e = setup_vec_t<OUT_BF16, 1>();
-    if (e == cudaSuccess) e = setup_vec_t<OUT_F16, 1>();
-    if (e == cudaSuccess) e = setup_vec_t<OUT_F32, 1>();
-    if (e == cudaSuccess) e = setup_vec_t<OUT_BF16, 2>();
-    if (e == cudaSuccess) e = setup_vec_t<OUT_F16, 2>();
-    if (e == cudaSuccess) e = setup_vec_t<OUT_F32, 2>();
+    cudaError_t e = setup_vec_w<false>();
+    if (e == cudaSuccess) e = setup_vec_w<true>();
     return e;
+}
+
+template <bool WIN>
+static cudaError_t launch_vec_w(const ConvLaunch &L, cudaStream_t stream)
+{
+    const int s = L.args.sw;
+    if (s == 1) {
+        if (L.out == OUT_BF16) return launch_vec_t<OUT_BF16, 1, WIN>(L, stream);
+        if (L.out == OUT_F16) return launch_vec_t<OUT_F16, 1, WIN>(L, stream);
+        if (L.out == OUT_F32) return launch_vec_t<OUT_F32, 1, WIN>(L, stream);
+    } else if (s == 2) {
+        if (L.out == OUT_BF16) return launch_vec_t<OUT_BF16, 2, WIN>(L, stream);
+        if (L.out == OUT_F16) return launch_vec_t<OUT_F16, 2, WIN>(L, stream);
+        if (L.out == OUT_F32) return launch_vec_t<OUT_F32, 2, WIN>(L, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_conv_vec(const ConvLaunch &L, cudaStream_t stream)
 {
-    const int s = L.args.sw;
-    if (s == 1) {
-        if (L.out == OUT_BF16) return launch_vec_t<OUT_BF16, 1>(L, stream);
-        if (L.out == OUT_F16) return launch_vec_t<OUT_F16, 1>(L, stream);
-        if (L.out == OUT_F32) return launch_vec_t<OUT_F32, 1>(L, stream);
-    } else if (s == 2) {
-        if (L.out == OUT_BF16) return launch_vec_t<OUT_BF16, 2>(L, stream);
-        if (L.out == OUT_F16) return launch_vec_t<OUT_F16, 2>(L, stream);
-        if (L.out == OUT_F32) return launch_vec_t<OUT_F32, 2>(L, stream);
-    }
-    return cudaErrorInvalidValue;
+    return L.args.win ? launch_vec_w<true>(L, stream) : launch_vec_w<false>(L, stream);
 }
 
 }  // namespace mmact

@@ -159,10 +159,7 @@ __global__ void __launch_bounds__(192, 1)
             int mb, nb;
             gemm_tile(t, p, mb, nb);
             const int n0 = nb * BN;
-            uint32_t got = 1;
-            if (lane == 0) got = epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase) ? 1u : 0u;
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (!got) { ok = false; break; }
+            if (!warp_epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t tbase = pp.tmem + ((uint32_t)(q * 32) << 16) + acc * TileN<BN>::ACC_STRIDE;
             const int row0 = mb * 128 + q * 32;

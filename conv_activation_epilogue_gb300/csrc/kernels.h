@@ -39,6 +39,10 @@ struct ConvArgs {
     int vec;             // 1: vectorised producer (conv_vec.cu), 0: per-element gather
     int TW, TH;          // vectorised path: output tile of TH rows x TW columns (TW * TH = 256)
     int tiles_oh, tiles_ow, W8;
+    int win;             // vectorised path: 1 = input window staged in smem by TMA (below)
+    int WB, HB, CB;      //   window box: WB columns x HB rows x CB channels
+    int rstep, rowmul;   //   window rows per filter row r, per output row of the tile
+    int raw_bytes;       //   bytes of one window
     int a_tma;           // 1: filter tiles by TMA, 0: gathered by the producer warps
     int y_tma;           // 1: output tiles by TMA store, 0: direct global stores
     int out_elem_bytes;
@@ -50,8 +54,11 @@ struct ConvArgs {
     unsigned long long wait_ns;
 };
 
+// Largest input window (bytes) the vectorised conv kernel stages per K block.
+constexpr int CONV_WIN_MAX_BYTES = 24576;
+
 struct ConvLaunch {
-    CUtensorMap tmW, tmY, tmY4;
+    CUtensorMap tmW, tmY, tmY4, tmX;
     ConvArgs args;
     int out;
     int grid;

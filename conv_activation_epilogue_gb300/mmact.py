@@ -27,7 +27,8 @@ _lib = None
 SYMBOLS = [
     "mmact_gemm", "mmact_gemm_split", "mmact_gemm_split_noalloc", "mmact_conv2d", "mmact_conv2d_split",
     "mmact_conv2d_nhwc",
-    "mmact_conv2d_out_shape", "mmact_get_last_error", "mmact_set_wait_timeout_ns",
+    "mmact_conv2d_out_shape", "mmact_conv2d_producer", "mmact_get_last_error",
+    "mmact_set_wait_timeout_ns",
     "mmact_selftest_wait_timeout", "mmact_set_gemm_tile_n", "mmact_status_string", "mmact_version",
 ]
 
@@ -62,6 +63,8 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     L.mmact_conv2d_nhwc.restype = ci
     L.mmact_conv2d_out_shape.argtypes = [i64, i64, i64, i64, p_i32, p_i32, p_i32,
                                          ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    L.mmact_conv2d_producer.argtypes = [i64] * 7 + [p_i32, p_i32, p_i32, ci, ci]
+    L.mmact_conv2d_producer.restype = ci
     L.mmact_get_last_error.argtypes = [vp]
     L.mmact_set_wait_timeout_ns.argtypes = [u64]
     L.mmact_set_wait_timeout_ns.restype = None
@@ -179,6 +182,19 @@ def mmact_conv2d_out_shape(H, W, kh, kw, stride, pads, dilation) -> tuple:
                                     _i32(dilation, 2), ctypes.byref(ho), ctypes.byref(wo)),
            "mmact_conv2d_out_shape")
     return ho.value, wo.value
+
+
+CONV_PRODUCER = {0: "gather", 1: "vector", 2: "window"}
+
+
+def mmact_conv2d_producer(N, C, H, W, Co, kh, kw, stride, pads, dilation, in_dtype, out_dtype) -> str:
+    """Which B-tile producer mmact_conv2d uses for this NCHW geometry (a name
+    from CONV_PRODUCER); dtypes are torch dtypes."""
+    r = load().mmact_conv2d_producer(N, C, H, W, Co, kh, kw, _i32(stride, 2), _i32(pads, 4),
+                                     _i32(dilation, 2), DTYPE[in_dtype], DTYPE[out_dtype])
+    if r not in CONV_PRODUCER:
+        raise ValueError("mmact_conv2d_producer: invalid arguments")
+    return CONV_PRODUCER[r]
 
 
 def _conv_args(x, w, bias, y, stride, pads, dilation):

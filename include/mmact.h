@@ -211,6 +211,24 @@ mmact_status mmact_conv2d_out_shape(int64_t H, int64_t W, int64_t kh, int64_t kw
                                     const int32_t dilations[2], int64_t *Ho, int64_t *Wo);
 
 /*
+ * Diagnostic: which B-tile producer mmact_conv2d (and mmact_conv2d_split)
+ * would use for this NCHW geometry.  The choice depends only on the shape and
+ * dtypes.  Returns a mmact_conv_producer value, or -1 when the arguments are
+ * invalid, C == 0, or the problem is too large for the library.
+ *   MMACT_CONV_GATHER  per-element im2col gather (any geometry)
+ *   MMACT_CONV_VECTOR  16-byte chunk loads from global memory + byte picks
+ *                      (W % 8 == 0, horizontal stride 1 or 2, filter rows a
+ *                      multiple of 16 bytes, output rows TMA-storable)
+ *   MMACT_CONV_WINDOW  as VECTOR, but each K block's input window is first
+ *                      loaded into shared memory by one TMA box (when that
+ *                      window fits in 24 KB)
+ */
+typedef enum { MMACT_CONV_GATHER = 0, MMACT_CONV_VECTOR = 1, MMACT_CONV_WINDOW = 2 } mmact_conv_producer;
+int mmact_conv2d_producer(int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh,
+                          int64_t kw, const int32_t strides[2], const int32_t pads[4],
+                          const int32_t dilations[2], mmact_dtype in_dtype, mmact_dtype out_dtype);
+
+/*
  * Synchronises `stream`, then reports and clears the current device's kernel
  * status word: MMACT_OK, MMACT_ERR_TIMEOUT (a bounded wait inside a kernel ran
  * out; the kernel skipped its remaining work and left its outputs

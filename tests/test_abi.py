@@ -65,6 +65,25 @@ def test_out_shape_matches_oracle(lib):
         assert Wo == orc.conv_out_dim(W, kw, st[1], pd[2], pd[3], dl[1])
 
 
+def test_conv_producer_choice(lib):
+    import torch
+    f16, bf16, f32 = torch.float16, torch.bfloat16, torch.float32
+    P = mmact.mmact_conv2d_producer
+    # the three conv workloads
+    assert P(8, 64, 56, 56, 128, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1), f16, f16) == "window"
+    assert P(16, 128, 64, 64, 256, 3, 3, (2, 2), (2, 2, 2, 2), (2, 2), bf16, bf16) == "window"
+    # 1x1, 64 channels per K block: the window would be 72 x 8 x 64 x 2 B > 24 KB
+    assert P(16, 128, 64, 64, 256, 1, 1, (2, 2), (0, 0, 0, 0), (1, 1), bf16, bf16) == "vector"
+    # input width not a multiple of 8, horizontal stride 3, K not a multiple of 8
+    assert P(2, 24, 17, 13, 40, 3, 3, (2, 2), (2, 2, 2, 2), (2, 2), bf16, bf16) == "gather"
+    assert P(1, 8, 16, 48, 8, 3, 3, (1, 3), (1, 1, 1, 1), (1, 1), f16, f16) == "gather"
+    assert P(3, 3, 11, 16, 5, 3, 2, (2, 1), (1, 0, 2, 1), (1, 2), f16, f32) == "gather"
+    # dh not a multiple of sh: the window keeps every input row
+    assert P(1, 16, 7, 16, 16, 3, 3, (2, 1), (1, 1, 2, 2), (1, 2), bf16, f16) == "window"
+    with pytest.raises(ValueError):
+        P(1, 8, 8, 8, 8, 0, 3, (1, 1), (0, 0, 0, 0), (1, 1), f16, f16)
+
+
 def test_out_shape_rejects_bad_geometry(lib):
     for args in [(5, 5, 0, 3, (1, 1), (0, 0, 0, 0), (1, 1)),
                  (5, 5, 3, 3, (0, 1), (0, 0, 0, 0), (1, 1)),

@@ -69,7 +69,24 @@ VEC_CASES = [
     (1, 40, 19, 48, 72, 3, 5, (1, 2), (0, 3, 2, 1), (2, 1), "f16", "f32"),       # asymmetric
     (3, 8, 10, 16, 24, 5, 5, (1, 1), (2, 2, 2, 2), (1, 1), "f16", "bf16"),       # K = 200
     (1, 16, 7, 16, 16, 3, 3, (2, 1), (1, 1, 2, 2), (1, 2), "bf16", "f16"),       # Wo = 16, Ho = 4
+    (1, 64, 32, 32, 64, 1, 1, (1, 1), (0, 0, 0, 0), (1, 1), "f16", "f16"),       # 1x1: global loads
+    (2, 20, 24, 40, 48, 2, 2, (1, 1), (0, 1, 1, 0), (1, 1), "bf16", "bf16"),     # 2x2: 17-channel window
+    (1, 16, 20, 24, 16, 7, 7, (1, 1), (3, 3, 3, 3), (1, 1), "f16", "f32"),       # 7x7 window
 ]
+
+# Producer each vectorised case takes (both vectorised producers must be covered).
+VEC_PRODUCERS = ["window", "window", "window", "vector", "window", "window", "window", "vector",
+                 "window", "window"]
+
+
+def test_vectorised_cases_cover_both_producers():
+    for case, want in zip(VEC_CASES, VEC_PRODUCERS, strict=True):
+        Nb, C, H, W, Co, kh, kw, st, pd, dl, dt, od = case
+        assert mmact.mmact_conv2d_producer(Nb, C, H, W, Co, kh, kw, st, pd, dl, TORCH[dt], TORCH[od]) == want, case
+    for case in CASES:
+        Nb, C, H, W, Co, kh, kw, st, pd, dl, dt, od = case
+        assert mmact.mmact_conv2d_producer(Nb, C, H, W, Co, kh, kw, st, pd, dl, TORCH[dt], TORCH[od]) in (
+            "gather", "window", "vector")
 
 
 @pytest.mark.parametrize("case", VEC_CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}x{c[3]}-{c[4]}k{c[5]}{c[6]}s{c[7][0]}{c[7][1]}")
