@@ -27,6 +27,7 @@ SOURCE = os.path.join(_HERE, "mmact_oracle.c")
 LIBRARY = os.path.join(_HERE, "liboracle.so")
 
 DTYPES = {"f16": 0, "bf16": 1}
+RES_DTYPES = {"f16": 0, "bf16": 1, "f32": 2}
 ACTS = {"none": 0, "relu": 1, "leaky_relu": 2, "tanh": 3, "sigmoid": 4, "gelu": 5}
 
 _build_lock = threading.Lock()
@@ -73,6 +74,10 @@ class Oracle:
         L.oracle_gemm.restype = ci
         L.oracle_conv2d.argtypes = [vp, vp, ci, vp] + [i64] * 15 + [ci, dbl, vp, i64, vp]
         L.oracle_conv2d.restype = ci
+        L.oracle_gemm_res.argtypes = [vp, vp, ci, vp, vp, ci, i64, i64, i64, ci, dbl, vp, i64, vp]
+        L.oracle_gemm_res.restype = ci
+        L.oracle_conv2d_res.argtypes = [vp, vp, ci, vp, vp, ci] + [i64] * 15 + [ci, dbl, vp, i64, vp]
+        L.oracle_conv2d_res.restype = ci
 
     # -- scalar pieces -----------------------------------------------------
     def decode(self, codes, dtype: str) -> np.ndarray:
@@ -114,11 +119,27 @@ class Oracle:
                 list(ex.map(work, range(threads)))
         return out
 
+    @staticmethod
+    def _residual(residual, res_dtype, count):
+        """(pointer, dtype code, keep-alive array) of an optional residual tensor."""
+        if residual is None:
+            return None, 0, None
+        if res_dtype == "f32":
+            r = np.ascontiguousarray(residual, dtype=np.float32)
+        else:
+            r = np.ascontiguousarray(residual, dtype=np.uint16)
+        if r.size != count:
+            raise ValueError("residual has the wrong number of elements")
+        return r.ctypes.data, RES_DTYPES[res_dtype], r
+
     def gemm(self, A, B, dtype: str, bias, act: str, alpha: float = 0.0,
-             points=None, threads: int | None = None) -> np.ndarray:
-        """act(A @ B + bias) in fp64 from 16-bit codes.
+             points=None, threads: int | None = None, residual=None,
+             res_dtype: str = "f32") -> np.ndarray:
+        """act(A @ B + bias [+ residual]) in fp64 from 16-bit codes.
 
         A: uint16 codes [M, K]; B: uint16 codes [K, N]; bias: float32 [N] or None.
+        residual: [M, N] uint16 codes (res_dtype f16 / bf16) or float32 values
+        (res_dtype f32), or None.
         points: flat indices i*N + j to evaluate (None = every element, returned
         as [M, N]).
         """
@@ -135,17 +156,22 @@ class Oracle:
         pts = np.arange(M * N, dtype=np.int64) if full else np.ascontiguousarray(points, dtype=np.int64)
         threads = threads or os.cpu_count() or 1
         bp = None if b is None else b.ctypes.data
+        rp, rd, _keep = self._residual(residual, res_dtype, M * N)
 
         def call(p, o):
-            return self.lib.oracle_gemm(A.ctypes.data, B.ctypes.data, DTYPES[dtype], bp, M, N, K,
-                                        ACTS[act], float(alpha), p.ctypes.data, p.shape[0], o.ctypes.data)
+            return self.lib.oracle_gemm_res(A.ctypes.data, B.ctypes.data, DTYPES[dtype], bp, rp, rd,
+                                            M, N, K, ACTS[act], float(alpha), p.ctypes.data,
+                                            p.shape[0], o.ctypes.data)
 
         out = self._run_chunks(call, pts, threads)
         return out.reshape(M, N) if full else out
 
     def conv2d(self, x, w, dtype: str, bias, stride, pads, dilation, act: str,
-               alpha: float = 0.0, points=None, threads: int | None = None) -> np.ndarray:
-        """act(conv2d(x, w) + bias) in fp64 from 16-bit codes.
+               alpha: float = 0.0, points=None, threads: int | None = None, residual=None,
+               res_dtype: str = "f32") -> np.ndarray:
+        """act(conv2d(x, w) + bias [+ residual]) in fp64 from 16-bit codes.
+
+        residual: [N, Co, Ho, Wo] in res_dtype (codes or float32 values), or None.
 
         x: [N, C, H, W] codes; w: [Co, C, kh, kw] codes; bias float32 [Co] or None;
         stride = (sh, sw); pads = (top, bottom, left, right); dilation = (dh, dw).
@@ -170,12 +196,13 @@ class Oracle:
         pts = np.arange(total, dtype=np.int64) if full else np.ascontiguousarray(points, dtype=np.int64)
         threads = threads or os.cpu_count() or 1
         bp = None if b is None else b.ctypes.data
+        rp, rd, _keep = self._residual(residual, res_dtype, total)
 
         def call(p, o):
-            return self.lib.oracle_conv2d(x.ctypes.data, w.ctypes.data, DTYPES[dtype], bp,
-                                          Nb, C, H, W, Co, kh, kw, sh, sw, pt, pb, pl, pr, dh, dw,
-                                          ACTS[act], float(alpha), p.ctypes.data, p.shape[0],
-                                          o.ctypes.data)
+            return self.lib.oracle_conv2d_res(x.ctypes.data, w.ctypes.data, DTYPES[dtype], bp, rp, rd,
+                                              Nb, C, H, W, Co, kh, kw, sh, sw, pt, pb, pl, pr, dh, dw,
+                                              ACTS[act], float(alpha), p.ctypes.data, p.shape[0],
+                                              o.ctypes.data)
 
         out = self._run_chunks(call, pts, threads)
         return out.reshape(Nb, Co, Ho, Wo) if full else out

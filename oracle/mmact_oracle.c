@@ -45,6 +45,15 @@
  *        print no formula, so this is the exact (erf) form, with C's erf() as
  *        the library step.
  *
+ *   RESIDUAL (optional, both operators)
+ *          z += R[same index],   then act(z)
+ *     -- "ops-nn fused_matmul_relu" article, section on the fusion families
+ *        (the element-wise "math" family): matmul + add + bias fused so that a
+ *        residual path is accumulated on chip instead of through HBM.  The page
+ *        gives no formula; the plain reading, in the order residual networks
+ *        use, adds R to the pre-activation: act(A x B + bias + R).  R has the
+ *        output's shape and dtype (fp16 / bf16 codes or fp32 values).
+ *
  * Input decoding follows the IEEE 754 binary16 definition (1 sign, 5 exponent
  * bits with bias 15, 10 fraction bits) and the bfloat16 definition (the upper
  * 16 bits of an IEEE binary32).
@@ -61,7 +70,7 @@
 #include <stdint.h>
 #include <string.h>
 
-enum { OR_F16 = 0, OR_BF16 = 1 };
+enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2 };
 enum { OR_ACT_NONE = 0, OR_ACT_RELU = 1, OR_ACT_LEAKY_RELU = 2, OR_ACT_TANH = 3,
        OR_ACT_SIGMOID = 4, OR_ACT_GELU = 5 };
 
@@ -102,6 +111,19 @@ double oracle_decode_bf16(uint16_t b)
 static double decode(uint16_t code, int dtype)
 {
     return dtype == OR_BF16 ? oracle_decode_bf16(code) : oracle_decode_f16(code);
+}
+
+/* Element idx of a residual tensor of dtype rdtype (16-bit codes or fp32). */
+static double residual_value(const void *R, int rdtype, int64_t idx)
+{
+    if (rdtype == OR_F32) return (double)((const float *)R)[idx];
+    return decode(((const uint16_t *)R)[idx], rdtype);
+}
+
+/* z plus residual element idx (z itself when there is no residual). */
+static double add_residual(double z, const void *R, int rdtype, int64_t idx)
+{
+    return R ? z + residual_value(R, rdtype, idx) : z;
 }
 
 /* tanh written out as the ratio of exponentials. */
@@ -148,28 +170,34 @@ static double gemm_z(const uint16_t *A, const uint16_t *B, int dtype, const floa
 }
 
 /*
- * A: [M,K] row-major codes; B: [K,N] row-major codes; bias: [N] fp32 or NULL.
+ * A: [M,K] row-major codes; B: [K,N] row-major codes; bias: [N] fp32 or NULL;
+ * R: residual [M,N] of dtype rdtype (OR_F16 / OR_BF16 codes, OR_F32 floats) or NULL.
  * points == NULL: out[i*N + j] for every element.  Otherwise out[p] is the
  * element at flat index points[p] (= i*N + j).  Returns 0, or -1 on a bad
  * argument.
  */
+int oracle_gemm_res(const uint16_t *A, const uint16_t *B, int dtype, const float *bias,
+                    const void *R, int rdtype, int64_t M, int64_t N, int64_t K, int act,
+                    double alpha, const int64_t *points, int64_t npoints, double *out)
+{
+    if (M < 0 || N < 0 || K < 0 || (dtype != OR_F16 && dtype != OR_BF16)) return -1;
+    if (R != NULL && rdtype != OR_F16 && rdtype != OR_BF16 && rdtype != OR_F32) return -1;
+    int64_t count = points ? npoints : M * N;
+    for (int64_t p = 0; p < count; ++p) {
+        int64_t idx = points ? points[p] : p;
+        if (idx < 0 || idx >= M * N) return -1;
+        double z = gemm_z(A, B, dtype, bias, N, K, idx / N, idx % N);
+        out[p] = oracle_act(add_residual(z, R, rdtype, idx), act, alpha);
+    }
+    return 0;
+}
+
+/* As oracle_gemm_res with no residual. */
 int oracle_gemm(const uint16_t *A, const uint16_t *B, int dtype, const float *bias,
                 int64_t M, int64_t N, int64_t K, int act, double alpha,
                 const int64_t *points, int64_t npoints, double *out)
 {
-    if (M < 0 || N < 0 || K < 0 || (dtype != OR_F16 && dtype != OR_BF16)) return -1;
-    if (points == NULL) {
-        for (int64_t i = 0; i < M; ++i)
-            for (int64_t j = 0; j < N; ++j)
-                out[i * N + j] = oracle_act(gemm_z(A, B, dtype, bias, N, K, i, j), act, alpha);
-        return 0;
-    }
-    for (int64_t p = 0; p < npoints; ++p) {
-        int64_t idx = points[p];
-        if (idx < 0 || idx >= M * N) return -1;
-        out[p] = oracle_act(gemm_z(A, B, dtype, bias, N, K, idx / N, idx % N), act, alpha);
-    }
-    return 0;
+    return oracle_gemm_res(A, B, dtype, bias, NULL, 0, M, N, K, act, alpha, points, npoints, out);
 }
 
 /* Output extent of one spatial axis. */
@@ -205,17 +233,20 @@ static double conv_z(const uint16_t *x, const uint16_t *w, int dtype, const floa
 }
 
 /*
- * x: [Nb,C,H,W] codes; w: [Co,C,kh,kw] codes; bias: [Co] fp32 or NULL.
+ * x: [Nb,C,H,W] codes; w: [Co,C,kh,kw] codes; bias: [Co] fp32 or NULL;
+ * R: residual [Nb,Co,Ho,Wo] of dtype rdtype, or NULL.
  * pads = (top, bottom, left, right).  y is [Nb,Co,Ho,Wo]; points are flat
  * indices into y (NULL = all).  Returns 0, or -1 on a bad argument.
  */
-int oracle_conv2d(const uint16_t *x, const uint16_t *w, int dtype, const float *bias,
-                  int64_t Nb, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
-                  int64_t sh, int64_t sw, int64_t pt, int64_t pb, int64_t pl, int64_t pr,
-                  int64_t dh, int64_t dw, int act, double alpha,
-                  const int64_t *points, int64_t npoints, double *out)
+int oracle_conv2d_res(const uint16_t *x, const uint16_t *w, int dtype, const float *bias,
+                      const void *R, int rdtype,
+                      int64_t Nb, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
+                      int64_t sh, int64_t sw, int64_t pt, int64_t pb, int64_t pl, int64_t pr,
+                      int64_t dh, int64_t dw, int act, double alpha,
+                      const int64_t *points, int64_t npoints, double *out)
 {
     if (dtype != OR_F16 && dtype != OR_BF16) return -1;
+    if (R != NULL && rdtype != OR_F16 && rdtype != OR_BF16 && rdtype != OR_F32) return -1;
     if (Nb < 0 || C < 0 || H < 0 || W < 0 || Co < 0 || kh <= 0 || kw <= 0) return -1;
     if (pt < 0 || pb < 0 || pl < 0 || pr < 0) return -1;
     conv_geom g = {Nb, C, H, W, Co, kh, kw, sh, sw, pt, pb, pl, pr, dh, dw, 0, 0};
@@ -231,7 +262,19 @@ int oracle_conv2d(const uint16_t *x, const uint16_t *w, int dtype, const float *
         int64_t oh = (idx / g.Wo) % g.Ho;
         int64_t co = (idx / (g.Wo * g.Ho)) % Co;
         int64_t n = idx / (g.Wo * g.Ho * Co);
-        out[p] = oracle_act(conv_z(x, w, dtype, bias, &g, n, co, oh, ow), act, alpha);
+        double z = conv_z(x, w, dtype, bias, &g, n, co, oh, ow);
+        out[p] = oracle_act(add_residual(z, R, rdtype, idx), act, alpha);
     }
     return 0;
+}
+
+/* As oracle_conv2d_res with no residual. */
+int oracle_conv2d(const uint16_t *x, const uint16_t *w, int dtype, const float *bias,
+                  int64_t Nb, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
+                  int64_t sh, int64_t sw, int64_t pt, int64_t pb, int64_t pl, int64_t pr,
+                  int64_t dh, int64_t dw, int act, double alpha,
+                  const int64_t *points, int64_t npoints, double *out)
+{
+    return oracle_conv2d_res(x, w, dtype, bias, NULL, 0, Nb, C, H, W, Co, kh, kw, sh, sw, pt, pb,
+                             pl, pr, dh, dw, act, alpha, points, npoints, out);
 }

@@ -234,6 +234,46 @@ def check_gemm_golden(orc):
     assert np.allclose(got, np.asarray(g["expected"]), rtol=1e-15, atol=0)
 
 
+def _res_values(R, res_dtype):
+    """Residual codes / values as float64, decoded with numpy (independent of the oracle)."""
+    R = np.asarray(R)
+    if res_dtype == "f32":
+        return R.astype(np.float32).astype(np.float64)
+    if res_dtype == "f16":
+        return R.astype(np.uint16).view(np.float16).astype(np.float64)
+    return (R.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def check_gemm_residual_identity(orc):
+    # B = I: the contraction is a copy, so C = act(A + bias + R) exactly
+    rng = np.random.default_rng(15)
+    M, K = 6, 5
+    for dtype, res_dtype in (("f16", "f16"), ("bf16", "bf16"), ("bf16", "f32")):
+        A = _rand_codes(rng, (M, K), dtype)
+        B = codes(np.eye(K), dtype)
+        bias = rng.uniform(-1, 1, K).astype(np.float32)
+        R = (rng.uniform(-2, 2, (M, K)).astype(np.float32) if res_dtype == "f32"
+             else _rand_codes(rng, (M, K), res_dtype, 2.0))
+        Ad = orc.decode(A, dtype)
+        for act, alpha in (("none", 0), ("relu", 0), ("leaky_relu", 0.3)):
+            got = orc.gemm(A, B, dtype, bias, act, alpha, residual=R, res_dtype=res_dtype)
+            exp = act_ref(Ad + bias.astype(np.float64)[None, :] + _res_values(R, res_dtype), act, alpha)
+            assert np.array_equal(got, exp), (dtype, res_dtype, act)
+
+
+def check_gemm_residual_golden(orc):
+    with open(os.path.join(GOLDEN, "gemm_2x2x2_residual_relu.json")) as f:
+        g = json.load(f)
+    A = codes(g["A"], g["dtype"])
+    B = codes(g["B"], g["dtype"])
+    R = codes(g["residual"], g["res_dtype"])
+    bias = np.asarray(g["bias"], dtype=np.float32)
+    z = orc.gemm(A, B, g["dtype"], bias, "none", residual=R, res_dtype=g["res_dtype"])
+    assert np.array_equal(z, np.asarray(g["z"]))
+    got = orc.gemm(A, B, g["dtype"], bias, g["act"], residual=R, res_dtype=g["res_dtype"])
+    assert np.array_equal(got, np.asarray(g["expected"]))
+
+
 # -------------------------------------------------------------------- conv --
 def check_conv_shape(orc):
     # the workloads' own shapes
@@ -377,10 +417,26 @@ def check_conv_golden(orc):
         assert np.allclose(y, exp, rtol=4e-15, atol=1e-15), name
 
 
+def check_conv_residual(orc):
+    # with no activation the residual enters linearly, element by element in y's own order
+    rng = np.random.default_rng(25)
+    x = _rand_codes(rng, (2, 3, 6, 7), "f16")
+    w = _rand_codes(rng, (4, 3, 3, 2), "f16")
+    bias = rng.uniform(-1, 1, 4).astype(np.float32)
+    geo = ((2, 1), (1, 0, 1, 1), (1, 2))
+    base = orc.conv2d(x, w, "f16", bias, *geo, "none")
+    R = _rand_codes(rng, base.shape, "bf16", 2.0)
+    got = orc.conv2d(x, w, "f16", bias, *geo, "none", residual=R, res_dtype="bf16")
+    assert np.array_equal(got, base + _res_values(R, "bf16"))
+    # and before the activation: tanh(z + R)
+    got = orc.conv2d(x, w, "f16", bias, *geo, "tanh", residual=R, res_dtype="bf16")
+    assert np.allclose(got, np.tanh(base + _res_values(R, "bf16")), rtol=4e-15, atol=1e-15)
+
+
 ALL_CHECKS = [
     check_decode_f16, check_decode_bf16, check_act_points, check_tanh, check_sigmoid, check_gelu,
     check_gemm_identity, check_gemm_permutation, check_gemm_ones, check_gemm_bruteforce,
-    check_gemm_points, check_gemm_golden,
+    check_gemm_points, check_gemm_golden, check_gemm_residual_identity, check_gemm_residual_golden,
     check_conv_shape, check_conv_bruteforce, check_conv_delta, check_conv_as_gemm,
-    check_conv_points, check_conv_golden,
+    check_conv_points, check_conv_golden, check_conv_residual,
 ]

@@ -37,6 +37,11 @@ MUTANTS = {
     "conv out-dim off by one": ("dil * (k - 1) - 1;", "dil * (k - 1);"),
     "conv skips padding check": ("if (ih < 0 || ih >= g->H || iw < 0 || iw >= g->W) continue;",
                                  "if (ih < 0 || iw < 0) continue;"),
+    "residual dropped": ("return R ? z + residual_value(R, rdtype, idx) : z;", "return z;"),
+    "residual after the activation": ("oracle_act(add_residual(z, R, rdtype, idx), act, alpha)",
+                                      "add_residual(oracle_act(z, act, alpha), R, rdtype, idx)"),
+    "residual codes read as bf16": ("return decode(((const uint16_t *)R)[idx], rdtype);",
+                                    "return decode(((const uint16_t *)R)[idx], OR_BF16);"),
     "f16 exponent bias": ("e - 15)", "e - 14)"),
     "f16 subnormal scale": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
     "bf16 fraction width": ("(double)f / 128.0", "(double)f / 256.0"),
