@@ -140,16 +140,17 @@ int choose_tile_n(int64_t tiles_m, int64_t N, int sms)
     return best;
 }
 
-// Shared by mmact_gemm and the first kernel of mmact_gemm_split.
+// Shared by mmact_gemm, mmact_gemm_residual and the first kernel of
+// mmact_gemm_split.  `res`: residual [M, N] in the output dtype, or null.
 mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void *C, int64_t M,
                           int64_t N, int64_t K, mmact_dtype ab, mmact_dtype cd, mmact_act act,
-                          float alpha, cudaStream_t stream)
+                          float alpha, cudaStream_t stream, const void *res = nullptr)
 {
     DeviceInfo *dev = nullptr;
     mmact_status st = device_info(&dev);
     if (st != MMACT_OK) return st;
     if (K == 0) {
-        cudaError_t e = launch_bias_act(bias, C, M, N, 0, N, out_kind(cd), (int)act, alpha, stream);
+        cudaError_t e = launch_bias_act(bias, C, M, N, 0, N, out_kind(cd), (int)act, alpha, stream, res);
         return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
     }
     GemmLaunch L;
@@ -171,6 +172,7 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
     a.act = (int)act;
     a.alpha = alpha;
     a.bias = bias;
+    a.res = res;
     a.status = dev->status;
     a.wait_ns = g_wait_ns.load();
     L.tile_n = bn;
@@ -494,6 +496,25 @@ MMACT_EXPORT mmact_status mmact_gemm(const void *A, const void *B, const float *
     if (M == 0 || N == 0) return MMACT_OK;
     return gemm_enqueue(A, B, bias, C, M, N, K, ab_dtype, c_dtype, act, alpha,
                         static_cast<cudaStream_t>(stream));
+}
+
+MMACT_EXPORT mmact_status mmact_gemm_residual(const void *A, const void *B, const float *bias,
+                                              const void *R, void *C, int64_t M, int64_t N, int64_t K,
+                                              mmact_dtype ab_dtype, mmact_dtype c_dtype, mmact_act act,
+                                              float alpha, void *stream)
+{
+    mmact_status s = gemm_check(A, B, bias, C, M, N, K, ab_dtype, c_dtype, act);
+    if (s != MMACT_OK) return s;
+    if (R == nullptr && M * N != 0) return MMACT_ERR_INVALID_ARG;
+    if (!aligned16(R)) return MMACT_ERR_UNSUPPORTED;
+    // R is read element by element before the same element of C is written,
+    // so R == C is allowed; any other overlap is not.
+    const int64_t bytes = M * N * elem_bytes(c_dtype);
+    const char *r = static_cast<const char *>(R), *c = static_cast<const char *>(C);
+    if (r != c && bytes != 0 && r < c + bytes && c < r + bytes) return MMACT_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return MMACT_OK;
+    return gemm_enqueue(A, B, bias, C, M, N, K, ab_dtype, c_dtype, act, alpha,
+                        static_cast<cudaStream_t>(stream), R);
 }
 
 MMACT_EXPORT mmact_status mmact_gemm_split(const void *A, const void *B, const float *bias, void *C,

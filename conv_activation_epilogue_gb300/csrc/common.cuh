@@ -184,11 +184,62 @@ __device__ void mma_role(const Pipe &pp, uint32_t sA, uint32_t sB, int num_tiles
     ptx::mbar_wait_bounded(pp.drain, 0, DRAIN_NS, nullptr);
 }
 
+// Two 16-bit output values (one 32-bit word, low half first) as floats.
+template <int OUT>
+__device__ __forceinline__ float2 unpack2(uint32_t w)
+{
+    if constexpr (OUT == OUT_BF16) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    } else {
+        __half2 h = *reinterpret_cast<__half2 *>(&w);
+        return __half22float2(h);
+    }
+}
+
+// Adds this lane's residual row segment -- COLS consecutive elements of the
+// output dtype starting at `res` -- to v[0..min(nvalid, COLS)).  Plain,
+// coherent loads (not the read-only path): the residual may be the output
+// tensor itself, each element read here before this unit's store writes it.
+template <int OUT, int COLS>
+__device__ __forceinline__ void add_residual(const void *res, int nvalid, float (&v)[COLS])
+{
+    if (nvalid >= COLS) {
+        const uint4 *q = reinterpret_cast<const uint4 *>(res);
+        constexpr int PER = OUT == OUT_F32 ? 4 : 8;      // elements per 16 bytes
+#pragma unroll
+        for (int c = 0; c < COLS / PER; ++c) {
+            const uint4 u = q[c];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if constexpr (OUT == OUT_F32) {
+                    v[4 * c + e] += __uint_as_float(w[e]);
+                } else {
+                    const float2 f = unpack2<OUT>(w[e]);
+                    v[8 * c + 2 * e] += f.x;
+                    v[8 * c + 2 * e + 1] += f.y;
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < COLS; ++j) {
+            if (j < nvalid) {
+                if constexpr (OUT == OUT_F32) v[j] += static_cast<const float *>(res)[j];
+                else if constexpr (OUT == OUT_BF16)
+                    v[j] += __bfloat162float(static_cast<const __nv_bfloat16 *>(res)[j]);
+                else v[j] += __half2float(static_cast<const __half *>(res)[j]);
+            }
+        }
+    }
+}
+
 // One epilogue unit: 32 rows (this warp's TMEM lane quarter) x one 128-byte
 // output row segment (32 fp32 or 64 16-bit columns).  Loads the fp32
 // accumulators from TMEM, adds the fp32 bias (per column from global memory
 // `bias_col[0..nvalid)`, zero beyond it or when null; or the per-row `brow`),
-// applies the activation in fp32, converts, and writes the row into a
+// adds the lane's residual row segment when `res` is not null, applies the
+// activation in fp32, converts, and writes the row into a
 // 32 x 128 B shared buffer in the 128-byte swizzled order a TMA store expects
 // (16-byte chunk c of row r lands at chunk c ^ (r & 7)).
 //
@@ -197,7 +248,8 @@ __device__ void mma_role(const Pipe &pp, uint32_t sA, uint32_t sB, int num_tiles
 // unswizzled map).
 template <int OUT, int ACT, bool BIAS_ROW, int NCOL = (OUT == OUT_F32 ? 32 : 64)>
 __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, int nvalid,
-                                         float brow, float alpha, uint32_t buf, int lane)
+                                         float brow, float alpha, uint32_t buf, int lane,
+                                         const void *res)
 {
     constexpr int COLS = NCOL;
     constexpr bool WIDE = COLS == 64;                  // two TMEM loads per unit
@@ -222,6 +274,7 @@ __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, 
         for (int j = 0; j < COLS; ++j)
             bc[j] = BIAS_ROW ? brow : ((bias_col != nullptr && j < nvalid) ? __ldg(bias_col + j) : 0.0f);
     }
+    if (res != nullptr) add_residual<OUT, COLS>(res, nvalid, bc);
     ptx::tmem_ld_wait(r0);
     if constexpr (WIDE) ptx::tmem_ld_wait(r1);
     if constexpr (OUT != OUT_F32 && !WIDE) {
@@ -274,26 +327,26 @@ __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, 
 template <int OUT, bool BIAS_ROW, int NCOL = (OUT == OUT_F32 ? 32 : 64)>
 __device__ __forceinline__ void epi_unit_dispatch(int act, uint32_t taddr, const float *bias_col,
                                                   int nvalid, float brow, float alpha, uint32_t buf,
-                                                  int lane)
+                                                  int lane, const void *res = nullptr)
 {
     switch (act) {
     case ACT_RELU:
-        epi_unit<OUT, ACT_RELU, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        epi_unit<OUT, ACT_RELU, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     case ACT_LEAKY:
-        epi_unit<OUT, ACT_LEAKY, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        epi_unit<OUT, ACT_LEAKY, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     case ACT_TANH:
-        epi_unit<OUT, ACT_TANH, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        epi_unit<OUT, ACT_TANH, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     case ACT_SIGMOID:
-        epi_unit<OUT, ACT_SIGMOID, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        epi_unit<OUT, ACT_SIGMOID, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     case ACT_GELU:
-        epi_unit<OUT, ACT_GELU, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        epi_unit<OUT, ACT_GELU, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     default:
-        epi_unit<OUT, ACT_NONE, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane);
+        epi_unit<OUT, ACT_NONE, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     }
 }

@@ -1,6 +1,7 @@
 // elementwise.cu -- the HBM-bound kernels: the second kernel of the two-kernel
 // ablation (fp32 workspace -> activation -> output dtype), the degenerate
-// empty-contraction case (output = act(bias)), and the bounded-wait self-test.
+// empty-contraction case (output = act(bias), plus the residual when one is
+// given), and the bounded-wait self-test.
 //
 // The ablation follows the "multimodal-ops Fused ConvTanh" article, section
 // on how the two kernels split the work: its second kernel reads the fp32
@@ -50,17 +51,26 @@ __global__ void __launch_bounds__(256) act_kernel(const float *__restrict__ ws, 
     }
 }
 
+template <int OUT>
+__device__ __forceinline__ float load_out(const void *p, int64_t k)
+{
+    if constexpr (OUT == OUT_F32) return static_cast<const float *>(p)[k];
+    else if constexpr (OUT == OUT_BF16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[k]);
+    else return __half2float(static_cast<const __half *>(p)[k]);
+}
+
 template <int OUT, int ACT>
 __global__ void __launch_bounds__(256) bias_act_kernel(const float *__restrict__ bias,
-                                                       void *__restrict__ out, int64_t rows,
+                                                       void *out, int64_t rows,
                                                        int64_t cols, int per_row, int64_t bias_len,
-                                                       float alpha)
+                                                       float alpha, const void *res)
 {
     const int64_t total = rows * cols;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total; k += stride) {
         const int64_t r = k / cols, c = k - r * cols;
-        const float b = bias == nullptr ? 0.0f : bias[per_row ? (r % bias_len) : c];
+        float b = bias == nullptr ? 0.0f : bias[per_row ? (r % bias_len) : c];
+        if (res != nullptr) b += load_out<OUT>(res, k);   // may alias out: read before the write
         const float v = act_f32<ACT>(b, alpha);
         if constexpr (OUT == OUT_F32) reinterpret_cast<float *>(out)[k] = v;
         else if constexpr (OUT == OUT_BF16) reinterpret_cast<__nv_bfloat16 *>(out)[k] = __float2bfloat16_rn(v);
@@ -113,11 +123,12 @@ cudaError_t launch_act(const float *ws, void *out, int64_t count, int out_kind, 
 template <int OUT>
 static cudaError_t launch_bias_act_o(const float *bias, void *out, int64_t rows, int64_t cols,
                                      int per_row, int64_t bias_len, int act, float alpha,
-                                     cudaStream_t s)
+                                     cudaStream_t s, const void *res)
 {
     const int64_t total = rows * cols;
     const int grid = (int)std::min<int64_t>((total + 255) / 256, 4096);
-#define MMACT_BA(A_) bias_act_kernel<OUT, A_><<<grid, 256, 0, s>>>(bias, out, rows, cols, per_row, bias_len, alpha)
+#define MMACT_BA(A_) \
+    bias_act_kernel<OUT, A_><<<grid, 256, 0, s>>>(bias, out, rows, cols, per_row, bias_len, alpha, res)
     switch (act) {
     case ACT_RELU: MMACT_BA(ACT_RELU); break;
     case ACT_LEAKY: MMACT_BA(ACT_LEAKY); break;
@@ -131,14 +142,15 @@ static cudaError_t launch_bias_act_o(const float *bias, void *out, int64_t rows,
 }
 
 cudaError_t launch_bias_act(const float *bias, void *out, int64_t rows, int64_t cols, int per_row,
-                            int64_t bias_len, int out_kind, int act, float alpha, cudaStream_t stream)
+                            int64_t bias_len, int out_kind, int act, float alpha, cudaStream_t stream,
+                            const void *res)
 {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
     if (out_kind == OUT_BF16)
-        return launch_bias_act_o<OUT_BF16>(bias, out, rows, cols, per_row, bias_len, act, alpha, stream);
+        return launch_bias_act_o<OUT_BF16>(bias, out, rows, cols, per_row, bias_len, act, alpha, stream, res);
     if (out_kind == OUT_F16)
-        return launch_bias_act_o<OUT_F16>(bias, out, rows, cols, per_row, bias_len, act, alpha, stream);
-    return launch_bias_act_o<OUT_F32>(bias, out, rows, cols, per_row, bias_len, act, alpha, stream);
+        return launch_bias_act_o<OUT_F16>(bias, out, rows, cols, per_row, bias_len, act, alpha, stream, res);
+    return launch_bias_act_o<OUT_F32>(bias, out, rows, cols, per_row, bias_len, act, alpha, stream, res);
 }
 
 cudaError_t launch_wait_selftest(unsigned int *status, unsigned long long timeout_ns,

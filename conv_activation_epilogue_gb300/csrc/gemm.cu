@@ -62,6 +62,16 @@ __device__ __forceinline__ void gemm_tile(int t, const GemmArgs &p, int &mb, int
 
 // tmCt: the map for the 32-column tail unit of a 224-wide tile with a 16-bit
 // output (unswizzled 64-byte rows); unused otherwise.
+// Start of output row `row`'s residual segment at column col0, or null (no
+// residual, or a row past M).
+template <int OUT>
+__device__ __forceinline__ const void *residual_row(const GemmArgs &p, int row, int col0)
+{
+    if (p.res == nullptr || row >= p.M) return nullptr;
+    constexpr int ESZ = OUT == OUT_F32 ? 4 : 2;
+    return static_cast<const char *>(p.res) + ((int64_t)row * p.N + col0) * ESZ;
+}
+
 template <int BN, int OUT>
 __global__ void __launch_bounds__(192, 1)
     gemm_act_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -171,7 +181,8 @@ __global__ void __launch_bounds__(192, 1)
                 const int col0 = n0 + u * COLS;
                 epi_unit_dispatch<OUT, false>(p.act, tbase + u * COLS,
                                               p.bias != nullptr ? p.bias + col0 : nullptr,
-                                              p.N - col0, 0.0f, p.alpha, buf, lane);
+                                              p.N - col0, 0.0f, p.alpha, buf, lane,
+                                              residual_row<OUT>(p, row0 + lane, col0));
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && row0 < p.M && col0 < p.N) {
@@ -188,7 +199,8 @@ __global__ void __launch_bounds__(192, 1)
                 const int col0 = n0 + (BN / COLS) * COLS;
                 epi_unit_dispatch<OUT, false, 32>(p.act, tbase + (BN / COLS) * COLS,
                                                   p.bias != nullptr ? p.bias + col0 : nullptr,
-                                                  p.N - col0, 0.0f, p.alpha, buf, lane);
+                                                  p.N - col0, 0.0f, p.alpha, buf, lane,
+                                                  residual_row<OUT>(p, row0 + lane, col0));
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && row0 < p.M && col0 < p.N) {

@@ -15,6 +15,7 @@ struct GemmArgs {
     int act;             // ACT_*
     float alpha;
     const float *bias;   // [N] or null
+    const void *res;     // residual [M, N] in the output dtype, or null
     unsigned int *status;
     unsigned long long wait_ns;
 };
@@ -108,9 +109,11 @@ cudaError_t launch_act(const float *ws, void *out, int64_t count, int out_kind, 
                        float alpha, int grid, cudaStream_t stream);
 // out[r][c] = act(bias[c]) (bias may be null) for an [rows x cols] output;
 // with per_row != 0 the bias runs along rows: out[r][c] = act(bias[r % bias_len]).
+// out = act(bias (+ res)) for the empty contraction; res, if not null, has
+// out's dtype and element order.
 cudaError_t launch_bias_act(const float *bias, void *out, int64_t rows, int64_t cols, int per_row,
                             int64_t bias_len, int out_kind, int act, float alpha,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const void *res = nullptr);
 cudaError_t launch_wait_selftest(unsigned int *status, unsigned long long timeout_ns,
                                  cudaStream_t stream);
 

@@ -25,7 +25,8 @@ _lib = None
 
 # Exported C symbols, as declared in include/mmact.h.
 SYMBOLS = [
-    "mmact_gemm", "mmact_gemm_split", "mmact_gemm_split_noalloc", "mmact_conv2d", "mmact_conv2d_split",
+    "mmact_gemm", "mmact_gemm_residual", "mmact_gemm_split", "mmact_gemm_split_noalloc", "mmact_conv2d",
+    "mmact_conv2d_split",
     "mmact_conv2d_nhwc",
     "mmact_conv2d_out_shape", "mmact_conv2d_producer", "mmact_get_last_error",
     "mmact_set_wait_timeout_ns",
@@ -53,6 +54,8 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
                                   ctypes.c_uint64, ctypes.c_int)
     p_i32 = ctypes.POINTER(i32)
     L.mmact_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, f32, vp]
+    L.mmact_gemm_residual.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, f32, vp]
+    L.mmact_gemm_residual.restype = ci
     L.mmact_gemm_split.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, f32, vp, vp]
     L.mmact_gemm_split_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, f32, vp]
     L.mmact_gemm_split_noalloc.restype = ci
@@ -140,6 +143,18 @@ def mmact_gemm(A, B, bias, C, act: str = "none", alpha: float = 0.0, stream=None
     pa, pb, pbias, pc, M, N, K = _gemm_args(A, B, bias, C)
     _check(L.mmact_gemm(pa, pb, pbias, pc, M, N, K, DTYPE[A.dtype], DTYPE[C.dtype], ACT[act],
                         float(alpha), _stream_handle(stream)), "mmact_gemm")
+
+
+def mmact_gemm_residual(A, B, bias, R, C, act: str = "none", alpha: float = 0.0, stream=None) -> None:
+    """C = act(A @ B + bias + R) in one fused kernel; R [M,N] has C's dtype and
+    may be C itself (see include/mmact.h)."""
+    L = load()
+    pa, pb, pbias, pc, M, N, K = _gemm_args(A, B, bias, C)
+    pr = _dev(R, "R", _OUT)
+    if tuple(R.shape) != (M, N) or R.dtype != C.dtype:
+        raise ValueError("R must be [M,N] with C's dtype")
+    _check(L.mmact_gemm_residual(pa, pb, pbias, pr, pc, M, N, K, DTYPE[A.dtype], DTYPE[C.dtype],
+                                 ACT[act], float(alpha), _stream_handle(stream)), "mmact_gemm_residual")
 
 
 def mmact_gemm_split(A, B, bias, C, workspace, act: str = "none", alpha: float = 0.0,

@@ -99,6 +99,23 @@ mmact_status mmact_gemm(const void *A, const void *B, const float *bias, void *C
                         mmact_act act, float alpha, void *stream);
 
 /*
+ * Fused GEMM + bias + residual + activation:  C = act(A x B + bias + R).
+ * The element-wise add of a residual tensor fused into the matmul epilogue,
+ * from the ops-nn fused_matmul_relu article's fusion families (the "math"
+ * family: matmul + add + bias, so a residual path is accumulated on chip
+ * instead of making a round trip through HBM); R is added to the fp32
+ * accumulator before the activation, the order residual networks use.
+ *   R  [M, N] in c_dtype, row-major, 16-byte aligned; read, never written.
+ *      R == C (in-place residual update) is allowed; any other overlap of
+ *      R and C returns MMACT_ERR_INVALID_ARG.  R may be NULL only if M*N == 0.
+ * Everything else as mmact_gemm (K == 0 gives C = act(bias + R)).
+ */
+mmact_status mmact_gemm_residual(const void *A, const void *B, const float *bias, const void *R,
+                                 void *C, int64_t M, int64_t N, int64_t K,
+                                 mmact_dtype ab_dtype, mmact_dtype c_dtype,
+                                 mmact_act act, float alpha, void *stream);
+
+/*
  * Two-kernel ablation of mmact_gemm.  Kernel 1 writes z = A x B + bias in fp32
  * to `workspace` ([M, N] fp32, caller-allocated, M*N*4 bytes, 16-byte
  * aligned); kernel 2 reads it, applies act in fp32 and writes C.  Same result

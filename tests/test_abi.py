@@ -134,6 +134,19 @@ def test_gemm_host_validation(lib):
     assert gemm(lib, split=True, ws=P16, M=0) == OK
 
 
+def test_gemm_residual_host_validation(lib):
+    E, U, OK = mmact.MMACT_ERR_INVALID_ARG, mmact.MMACT_ERR_UNSUPPORTED, mmact.MMACT_OK
+
+    def res(R=P16 + 4096, C=P16, M=16, N=16, K=16, cd=1):
+        return lib.mmact_gemm_residual(P16, P16, None, R, C, M, N, K, 1, cd, 1, ctypes.c_float(0), None)
+
+    assert res(R=None) == E                  # the residual is required
+    assert res(R=None, M=0) == OK            # ... unless the output is empty
+    assert res(R=P_MIS) == U                 # 16-byte alignment
+    assert res(R=P16 + 16) == E              # partial overlap with C (16x16 bf16 = 512 B)
+    assert res(M=-1) == E
+
+
 def test_conv_host_validation(lib):
     E, U = mmact.MMACT_ERR_INVALID_ARG, mmact.MMACT_ERR_UNSUPPORTED
     i32 = lambda *v: (ctypes.c_int32 * len(v))(*v)  # noqa: E731
