@@ -165,6 +165,42 @@ __global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
 
     const uint32_t sA = base + Cfg::OFF_A, sB = base + Cfg::OFF_B;
 
+    // One epilogue unit: 32 output channels (this warp's TMEM lane quarter,
+    // starting at co_row0) x COLS pixels of the tile, from accumulator column
+    // tbase + u * COLS, staged in `buf` and stored by TMA.
+    auto store_unit = [&](int n, int toh, int tow, int co_row0, float brow, uint32_t tbase, int u,
+                          uint32_t buf) {
+        epi_unit_dispatch<OUT, true>(p.act, tbase + u * COLS, nullptr, 0, brow, p.alpha, buf, lane);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && co_row0 < p.Co) {
+            const int col = u * COLS;                    // first B-tile column of this unit
+            if (p.TW == 32) {
+                // the tile is 256 consecutive pixels of image n
+                const int pix0 = toh * p.TH * p.Wo + col;
+                if (pix0 < p.P) {
+                    ptx::tma_store_3d(&tmY, buf, pix0, co_row0, n);
+                    ptx::bulk_commit();
+                }
+            } else {
+                const int oh = toh * p.TH + col / 64;
+                const int ow = tow * 64 + (col & 63);
+                if (oh < p.Ho && ow < p.Wo) {
+                    ptx::tma_store_4d(&tmY4, buf, ow, oh, co_row0, n);
+                    ptx::bulk_commit();
+                }
+            }
+        }
+    };
+
+    // The CTA's last tile: its accumulator buffer and phase, and the number of
+    // warps sharing its epilogue (each CTA of a small conv owns one tile, so
+    // that epilogue is not hidden behind any main loop: the gather warps, idle
+    // by then, take two of every three units).
+    const int my_tiles = blockIdx.x < (unsigned)p.num_tiles
+                             ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int t_last = (int)blockIdx.x + (my_tiles - 1) * (int)gridDim.x;
+
     if (warp == 0) {
         if (lane == 0) {
             // ---------------------------------------------- filter producer --
@@ -299,6 +335,38 @@ __global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
                 if (++rst == (uint32_t)Cfg::RSTAGES) { rst = 0; rph ^= 1u; }
             }
         }
+        if (ok && my_tiles > 0) {
+            // ------------------------------- help with the last tile's epilogue --
+            // Gather warp g (lane quarter g & 3) takes units u = 1 + (g >> 2)
+            // (mod 3) of the CTA's last tile, staged in the operand ring, which
+            // no MMA reads any more once that tile's accumulator is complete.
+            const int hq = warp & 3, hslot = 1 + ((warp - 6) >> 2);
+            const uint32_t hacc = (uint32_t)((my_tiles - 1) & 1);
+            const uint32_t hphase = (uint32_t)(((my_tiles - 1) >> 1) & 1);
+            int n, toh, tow, cb;
+            vconv_tile(t_last, p, n, toh, tow, cb);
+            const int co_row0 = cb * 128 + hq * 32;
+            const int co = co_row0 + lane;
+            const float brow = (p.bias != nullptr && co < p.Co) ? __ldg(p.bias + co) : 0.0f;
+            if (warp_epi_wait(pp, pp.tfull0 + 8 * hacc, hphase)) {
+                ptx::tc_fence_after();
+                const uint32_t tbase = pp.tmem + ((uint32_t)(hq * 32) << 16) + hacc * BN;
+                const uint32_t hbuf = sB + (uint32_t)(warp - 6) * 8192u;
+                uint32_t hunits = 0;
+#pragma unroll 1
+                for (int u = hslot; u < BN / COLS; u += 3) {
+                    const uint32_t buf = hbuf + (hunits++ & 1u) * 4096u;
+                    if (lane == 0) ptx::bulk_wait_read<1>();
+                    __syncwarp();
+                    store_unit(n, toh, tow, co_row0, brow, tbase, u, buf);
+                }
+                ptx::tc_fence_before();
+                if (lane == 0) ptx::bulk_wait<0>();
+                __syncwarp();
+            } else {
+                ok = false;
+            }
+        }
         if (!ok) pipe_fail(pp);
     } else if (warp >= 6) {
         // ---------------------------------------------------- B-tile gather --
@@ -390,6 +458,38 @@ __global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
+        if (ok && my_tiles > 0) {
+            // ------------------------------- help with the last tile's epilogue --
+            // Gather warp g (lane quarter g & 3) takes units u = 1 + (g >> 2)
+            // (mod 3) of the CTA's last tile, staged in the operand ring, which
+            // no MMA reads any more once that tile's accumulator is complete.
+            const int hq = warp & 3, hslot = 1 + ((warp - 6) >> 2);
+            const uint32_t hacc = (uint32_t)((my_tiles - 1) & 1);
+            const uint32_t hphase = (uint32_t)(((my_tiles - 1) >> 1) & 1);
+            int n, toh, tow, cb;
+            vconv_tile(t_last, p, n, toh, tow, cb);
+            const int co_row0 = cb * 128 + hq * 32;
+            const int co = co_row0 + lane;
+            const float brow = (p.bias != nullptr && co < p.Co) ? __ldg(p.bias + co) : 0.0f;
+            if (warp_epi_wait(pp, pp.tfull0 + 8 * hacc, hphase)) {
+                ptx::tc_fence_after();
+                const uint32_t tbase = pp.tmem + ((uint32_t)(hq * 32) << 16) + hacc * BN;
+                const uint32_t hbuf = sB + (uint32_t)(warp - 6) * 8192u;
+                uint32_t hunits = 0;
+#pragma unroll 1
+                for (int u = hslot; u < BN / COLS; u += 3) {
+                    const uint32_t buf = hbuf + (hunits++ & 1u) * 4096u;
+                    if (lane == 0) ptx::bulk_wait_read<1>();
+                    __syncwarp();
+                    store_unit(n, toh, tow, co_row0, brow, tbase, u, buf);
+                }
+                ptx::tc_fence_before();
+                if (lane == 0) ptx::bulk_wait<0>();
+                __syncwarp();
+            } else {
+                ok = false;
+            }
+        }
         if (!ok) pipe_fail(pp);
     } else {
         // -------------------------------------------------------- epilogue --
@@ -406,32 +506,13 @@ __global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
             if (!warp_epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t tbase = pp.tmem + ((uint32_t)(qd * 32) << 16) + acc * BN;
+            const int ustep = t == t_last ? 3 : 1;      // last tile: units 0, 3, 6 (helpers: the rest)
 #pragma unroll 1
-            for (int u = 0; u < BN / COLS; ++u) {
+            for (int u = 0; u < BN / COLS; u += ustep) {
                 const uint32_t buf = my_buf + (units++ & 1u) * 4096u;
                 if (lane == 0) ptx::bulk_wait_read<1>();
                 __syncwarp();
-                epi_unit_dispatch<OUT, true>(p.act, tbase + u * COLS, nullptr, 0, brow, p.alpha, buf, lane);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && co_row0 < p.Co) {
-                    const int col = u * COLS;                // first B-tile column of this unit
-                    if (p.TW == 32) {
-                        // the tile is 256 consecutive pixels of image n
-                        const int pix0 = toh * p.TH * p.Wo + col;
-                        if (pix0 < p.P) {
-                            ptx::tma_store_3d(&tmY, buf, pix0, co_row0, n);
-                            ptx::bulk_commit();
-                        }
-                    } else {
-                        const int oh = toh * p.TH + col / 64;
-                        const int ow = tow * 64 + (col & 63);
-                        if (oh < p.Ho && ow < p.Wo) {
-                            ptx::tma_store_4d(&tmY4, buf, ow, oh, co_row0, n);
-                            ptx::bulk_commit();
-                        }
-                    }
-                }
+                store_unit(n, toh, tow, co_row0, brow, tbase, u, buf);
             }
             ptx::tc_fence_before();
             __syncwarp();
