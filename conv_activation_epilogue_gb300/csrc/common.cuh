@@ -63,6 +63,27 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     }
 }
 
+// Launches `kernel` with programmatic stream serialization: the next kernel
+// in the stream may begin its set-up (barrier init, TMEM allocation,
+// tensor-map prefetch) while this one finishes, and every kernel of this
+// library waits in ptx::griddep_wait() before it touches global data.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Shared-memory addresses of the pipeline's barriers and flags.
 struct Pipe {
     uint32_t full0, empty0;      // operand ring: barrier s at +8*s

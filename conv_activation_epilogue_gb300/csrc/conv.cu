@@ -81,6 +81,12 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const uint32_t base = ptx::smem_addr(smem);
+    // let the next kernel in the stream start its set-up; fetch the tensor
+    // maps while this one sets up
+    ptx::griddep_launch_dependents();
+    if (threadIdx.x == 0) {
+        if (p.a_tma) ptx::prefetch_tensormap(&tmW);
+    }
     if (base & 1023u) {
         if (threadIdx.x == 0) atomicOr(p.status, ST_SMEM_ALIGN);
         return;
@@ -119,6 +125,7 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
     ptx::cta_sync();
     ptx::tc_fence_after();
     pp.tmem = misc[0];
+    ptx::griddep_wait();   // inputs and outputs may belong to the previous kernel
 
     const uint32_t sA = base + Cfg::OFF_A, sB = base + Cfg::OFF_B;
 
@@ -285,9 +292,8 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
 template <int OUT>
 static cudaError_t launch_conv_t(const ConvLaunch &L, cudaStream_t stream)
 {
-    conv_act_kernel<OUT><<<L.grid, ConvCfg::THREADS, ConvCfg::SMEM_BYTES, stream>>>(L.tmW, L.tmY,
-                                                                                    L.args);
-    return cudaGetLastError();
+    return launch_k(conv_act_kernel<OUT>, L.grid, ConvCfg::THREADS, ConvCfg::SMEM_BYTES, stream, L.tmW,
+                    L.tmY, L.args);
 }
 
 cudaError_t setup_conv_kernels()

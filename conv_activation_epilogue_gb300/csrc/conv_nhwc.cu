@@ -78,6 +78,13 @@ __global__ void __launch_bounds__(NhwcCfg<BN>::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const uint32_t base = ptx::smem_addr(smem);
+    // let the next kernel in the stream start its set-up; fetch the tensor
+    // maps while this one sets up
+    ptx::griddep_launch_dependents();
+    if (threadIdx.x == 0) {
+        ptx::prefetch_tensormap(&tmX);
+        ptx::prefetch_tensormap(&tmW);
+    }
     if (base & 1023u) {
         if (threadIdx.x == 0) atomicOr(p.status, ST_SMEM_ALIGN);
         return;
@@ -114,6 +121,7 @@ __global__ void __launch_bounds__(NhwcCfg<BN>::THREADS, 1)
     ptx::cta_sync();
     ptx::tc_fence_after();
     pp.tmem = misc[0];
+    ptx::griddep_wait();   // inputs and outputs may belong to the previous kernel
 
     const uint32_t sA = base + Cfg::OFF_A, sB = base + Cfg::OFF_B;
 
@@ -213,9 +221,8 @@ __global__ void __launch_bounds__(NhwcCfg<BN>::THREADS, 1)
 template <int BN, int OUT>
 static cudaError_t launch_nhwc_t(const NhwcLaunch &L, cudaStream_t stream)
 {
-    conv_nhwc_kernel<BN, OUT><<<L.grid, NhwcCfg<BN>::THREADS, NhwcCfg<BN>::SMEM_BYTES, stream>>>(
-        L.tmX, L.tmW, L.tmY, L.args);
-    return cudaGetLastError();
+    return launch_k(conv_nhwc_kernel<BN, OUT>, L.grid, NhwcCfg<BN>::THREADS, NhwcCfg<BN>::SMEM_BYTES,
+                    stream, L.tmX, L.tmW, L.tmY, L.args);
 }
 
 template <int BN, int OUT>

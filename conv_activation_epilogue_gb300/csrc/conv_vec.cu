@@ -120,6 +120,13 @@ __global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const uint32_t base = ptx::smem_addr(smem);
+    // let the next kernel in the stream start its set-up; fetch the tensor
+    // maps while this one sets up
+    ptx::griddep_launch_dependents();
+    if (threadIdx.x == 0) {
+        ptx::prefetch_tensormap(&tmW);
+        if constexpr (WIN) ptx::prefetch_tensormap(&tmX);
+    }
     if (base & 1023u) {
         if (threadIdx.x == 0) atomicOr(p.status, ST_SMEM_ALIGN);
         return;
@@ -162,6 +169,7 @@ __global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
     ptx::cta_sync();
     ptx::tc_fence_after();
     pp.tmem = misc[0];
+    ptx::griddep_wait();   // inputs and outputs may belong to the previous kernel
 
     const uint32_t sA = base + Cfg::OFF_A, sB = base + Cfg::OFF_B;
 
@@ -542,9 +550,8 @@ template <int OUT, int S, bool WIN>
 static cudaError_t launch_vec_t(const ConvLaunch &L, cudaStream_t stream)
 {
     using Cfg = ConvVecCfg<WIN>;
-    conv_vec_kernel<OUT, S, WIN><<<L.grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(L.tmW, L.tmY, L.tmY4,
-                                                                                      L.tmX, L.args);
-    return cudaGetLastError();
+    return launch_k(conv_vec_kernel<OUT, S, WIN>, L.grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream, L.tmW,
+                    L.tmY, L.tmY4, L.tmX, L.args);
 }
 
 template <int OUT, int S, bool WIN>

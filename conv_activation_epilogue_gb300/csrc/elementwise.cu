@@ -19,6 +19,8 @@ template <int OUT, int ACT>
 __global__ void __launch_bounds__(256) act_kernel(const float *__restrict__ ws, void *__restrict__ out,
                                                   int64_t count, float alpha)
 {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the workspace is the previous kernel's output
     const int64_t n8 = count >> 3;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const float4 *src = reinterpret_cast<const float4 *>(ws);
@@ -65,6 +67,8 @@ __global__ void __launch_bounds__(256) bias_act_kernel(const float *__restrict__
                                                        int64_t cols, int per_row, int64_t bias_len,
                                                        float alpha, const void *res)
 {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
     const int64_t total = rows * cols;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total; k += stride) {
@@ -82,6 +86,8 @@ __global__ void __launch_bounds__(256) bias_act_kernel(const float *__restrict__
 // and record the timeout in the status word.
 __global__ void wait_selftest_kernel(unsigned int *status, unsigned long long timeout_ns)
 {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t abort_flag;
     const uint32_t b = ptx::smem_addr(&bar);
@@ -101,14 +107,13 @@ static cudaError_t launch_act_o(const float *ws, void *out, int64_t count, int a
                                 int grid, cudaStream_t s)
 {
     switch (act) {
-    case ACT_RELU: act_kernel<OUT, ACT_RELU><<<grid, 256, 0, s>>>(ws, out, count, alpha); break;
-    case ACT_LEAKY: act_kernel<OUT, ACT_LEAKY><<<grid, 256, 0, s>>>(ws, out, count, alpha); break;
-    case ACT_TANH: act_kernel<OUT, ACT_TANH><<<grid, 256, 0, s>>>(ws, out, count, alpha); break;
-    case ACT_SIGMOID: act_kernel<OUT, ACT_SIGMOID><<<grid, 256, 0, s>>>(ws, out, count, alpha); break;
-    case ACT_GELU: act_kernel<OUT, ACT_GELU><<<grid, 256, 0, s>>>(ws, out, count, alpha); break;
-    default: act_kernel<OUT, ACT_NONE><<<grid, 256, 0, s>>>(ws, out, count, alpha); break;
+    case ACT_RELU: return launch_k(act_kernel<OUT, ACT_RELU>, grid, 256, 0, s, ws, out, count, alpha);
+    case ACT_LEAKY: return launch_k(act_kernel<OUT, ACT_LEAKY>, grid, 256, 0, s, ws, out, count, alpha);
+    case ACT_TANH: return launch_k(act_kernel<OUT, ACT_TANH>, grid, 256, 0, s, ws, out, count, alpha);
+    case ACT_SIGMOID: return launch_k(act_kernel<OUT, ACT_SIGMOID>, grid, 256, 0, s, ws, out, count, alpha);
+    case ACT_GELU: return launch_k(act_kernel<OUT, ACT_GELU>, grid, 256, 0, s, ws, out, count, alpha);
+    default: return launch_k(act_kernel<OUT, ACT_NONE>, grid, 256, 0, s, ws, out, count, alpha);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_act(const float *ws, void *out, int64_t count, int out_kind, int act, float alpha,
@@ -128,14 +133,15 @@ static cudaError_t launch_bias_act_o(const float *bias, void *out, int64_t rows,
     const int64_t total = rows * cols;
     const int grid = (int)std::min<int64_t>((total + 255) / 256, 4096);
 #define MMACT_BA(A_) \
-    bias_act_kernel<OUT, A_><<<grid, 256, 0, s>>>(bias, out, rows, cols, per_row, bias_len, alpha, res)
+    return launch_k(bias_act_kernel<OUT, A_>, grid, 256, 0, s, bias, out, rows, cols, per_row, bias_len, \
+                    alpha, res)
     switch (act) {
-    case ACT_RELU: MMACT_BA(ACT_RELU); break;
-    case ACT_LEAKY: MMACT_BA(ACT_LEAKY); break;
-    case ACT_TANH: MMACT_BA(ACT_TANH); break;
-    case ACT_SIGMOID: MMACT_BA(ACT_SIGMOID); break;
-    case ACT_GELU: MMACT_BA(ACT_GELU); break;
-    default: MMACT_BA(ACT_NONE); break;
+    case ACT_RELU: MMACT_BA(ACT_RELU);
+    case ACT_LEAKY: MMACT_BA(ACT_LEAKY);
+    case ACT_TANH: MMACT_BA(ACT_TANH);
+    case ACT_SIGMOID: MMACT_BA(ACT_SIGMOID);
+    case ACT_GELU: MMACT_BA(ACT_GELU);
+    default: MMACT_BA(ACT_NONE);
     }
 #undef MMACT_BA
     return cudaGetLastError();
@@ -156,8 +162,7 @@ cudaError_t launch_bias_act(const float *bias, void *out, int64_t rows, int64_t 
 cudaError_t launch_wait_selftest(unsigned int *status, unsigned long long timeout_ns,
                                  cudaStream_t stream)
 {
-    wait_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
-    return cudaGetLastError();
+    return launch_k(wait_selftest_kernel, 1, 32, 0, stream, status, timeout_ns);
 }
 
 }  // namespace mmact

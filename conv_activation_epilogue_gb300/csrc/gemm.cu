@@ -85,6 +85,13 @@ __global__ void __launch_bounds__(192, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const uint32_t base = ptx::smem_addr(smem);
+    // let the next kernel in the stream start its set-up; fetch the tensor
+    // maps while this one sets up
+    ptx::griddep_launch_dependents();
+    if (threadIdx.x == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+    }
     if (base & 1023u) {   // the swizzle patterns assume a 1024-byte aligned ring
         if (threadIdx.x == 0) atomicOr(p.status, ST_SMEM_ALIGN);
         return;
@@ -121,6 +128,7 @@ __global__ void __launch_bounds__(192, 1)
     ptx::cta_sync();
     ptx::tc_fence_after();
     pp.tmem = misc[0];
+    ptx::griddep_wait();   // inputs and outputs may belong to the previous kernel
 
     const uint32_t sA = base + Cfg::OFF_A, sB = base + Cfg::OFF_B;
 
@@ -235,9 +243,8 @@ __global__ void __launch_bounds__(192, 1)
 template <int BN, int OUT>
 static cudaError_t launch_gemm_t(const GemmLaunch &L, cudaStream_t stream)
 {
-    gemm_act_kernel<BN, OUT><<<L.grid, 192, GemmCfg<BN>::SMEM_BYTES, stream>>>(L.tmA, L.tmB, L.tmC,
-                                                                                L.tmCt, L.args);
-    return cudaGetLastError();
+    return launch_k(gemm_act_kernel<BN, OUT>, L.grid, 192, GemmCfg<BN>::SMEM_BYTES, stream, L.tmA, L.tmB,
+                    L.tmC, L.tmCt, L.args);
 }
 
 template <int BN, int OUT>

@@ -29,6 +29,23 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
+// ----------------------------------------------- programmatic dependent launch --
+// Lets the next kernel in the stream be scheduled now (its blocks still wait
+// in griddep_wait until this grid has finished).  No effect when the launch
+// carried no programmatic-serialization attribute.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until every grid this one depends on has completed and its memory
+// operations are visible.  Must precede the first access to data an earlier
+// kernel in the stream may write (inputs) or read (outputs).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier --
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
