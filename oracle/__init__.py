@@ -26,7 +26,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "mmact_oracle.c")
 LIBRARY = os.path.join(_HERE, "liboracle.so")
 
-DTYPES = {"f16": 0, "bf16": 1}
+DTYPES = {"f16": 0, "bf16": 1, "f32": 2}
 RES_DTYPES = {"f16": 0, "bf16": 1, "f32": 2}
 ACTS = {"none": 0, "relu": 1, "leaky_relu": 2, "tanh": 3, "sigmoid": 4, "gelu": 5}
 
@@ -132,19 +132,25 @@ class Oracle:
             raise ValueError("residual has the wrong number of elements")
         return r.ctypes.data, RES_DTYPES[res_dtype], r
 
+    @staticmethod
+    def _inputs(dtype, *arrays):
+        """16-bit codes as uint16, fp32 inputs as float32 (C-contiguous)."""
+        kind = np.float32 if dtype == "f32" else np.uint16
+        return [np.ascontiguousarray(a, dtype=kind) for a in arrays]
+
     def gemm(self, A, B, dtype: str, bias, act: str, alpha: float = 0.0,
              points=None, threads: int | None = None, residual=None,
              res_dtype: str = "f32") -> np.ndarray:
         """act(A @ B + bias [+ residual]) in fp64 from 16-bit codes.
 
-        A: uint16 codes [M, K]; B: uint16 codes [K, N]; bias: float32 [N] or None.
+        A: [M, K]; B: [K, N] -- uint16 codes for dtype f16 / bf16, float32
+        values for dtype f32; bias: float32 [N] or None.
         residual: [M, N] uint16 codes (res_dtype f16 / bf16) or float32 values
         (res_dtype f32), or None.
         points: flat indices i*N + j to evaluate (None = every element, returned
         as [M, N]).
         """
-        A = np.ascontiguousarray(A, dtype=np.uint16)
-        B = np.ascontiguousarray(B, dtype=np.uint16)
+        A, B = self._inputs(dtype, A, B)
         M, K = A.shape
         K2, N = B.shape
         if K2 != K:
@@ -173,12 +179,12 @@ class Oracle:
 
         residual: [N, Co, Ho, Wo] in res_dtype (codes or float32 values), or None.
 
-        x: [N, C, H, W] codes; w: [Co, C, kh, kw] codes; bias float32 [Co] or None;
+        x: [N, C, H, W]; w: [Co, C, kh, kw] -- codes for f16 / bf16, float32
+        values for f32; bias float32 [Co] or None;
         stride = (sh, sw); pads = (top, bottom, left, right); dilation = (dh, dw).
         points: flat indices into y [N, Co, Ho, Wo] (None = all, returned 4-D).
         """
-        x = np.ascontiguousarray(x, dtype=np.uint16)
-        w = np.ascontiguousarray(w, dtype=np.uint16)
+        x, w = self._inputs(dtype, x, w)
         Nb, C, H, W = x.shape
         Co, C2, kh, kw = w.shape
         if C2 != C:

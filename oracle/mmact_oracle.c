@@ -8,7 +8,8 @@
  * header, table or helper with the CUDA path; the two meet only through the
  * seeded input bytes that both consume.
  *
- * What it computes (fp64 throughout, over the exact 16-bit input values):
+ * What it computes (fp64 throughout, over the exact input values: fp16 / bf16
+ * codes, or fp32 values for the fp32-input variants):
  *
  *   GEMM   z[i][j] = (sum_{t<K} A[i][t] * B[t][j]) + bias[j]
  *          C[i][j] = act(z[i][j])
@@ -56,7 +57,10 @@
  *
  * Input decoding follows the IEEE 754 binary16 definition (1 sign, 5 exponent
  * bits with bias 15, 10 fraction bits) and the bfloat16 definition (the upper
- * 16 bits of an IEEE binary32).
+ * 16 bits of an IEEE binary32); fp32 inputs are widened to fp64 exactly.  The
+ * fp32 variants (the Fused ConvTanh article's evaluation covers fp32 cases
+ * beside fp16 and bf16) are still defined on the exact fp32 values: any
+ * reduced-precision arithmetic on the GPU side is the GPU's error.
  *
  * Each output element is computed on its own, from the definition, with the
  * sum over t (GEMM) or (ci, r, q) (conv) taken in ascending order.  Callers
@@ -113,11 +117,22 @@ static double decode(uint16_t code, int dtype)
     return dtype == OR_BF16 ? oracle_decode_bf16(code) : oracle_decode_f16(code);
 }
 
+/* Element idx of an input tensor: 16-bit codes (OR_F16 / OR_BF16) or fp32 values (OR_F32). */
+static double in_value(const void *p, int dtype, int64_t idx)
+{
+    if (dtype == OR_F32) return (double)((const float *)p)[idx];
+    return decode(((const uint16_t *)p)[idx], dtype);
+}
+
+static int valid_in_dtype(int dtype)
+{
+    return dtype == OR_F16 || dtype == OR_BF16 || dtype == OR_F32;
+}
+
 /* Element idx of a residual tensor of dtype rdtype (16-bit codes or fp32). */
 static double residual_value(const void *R, int rdtype, int64_t idx)
 {
-    if (rdtype == OR_F32) return (double)((const float *)R)[idx];
-    return decode(((const uint16_t *)R)[idx], rdtype);
+    return in_value(R, rdtype, idx);
 }
 
 /* z plus residual element idx (z itself when there is no residual). */
@@ -160,28 +175,29 @@ double oracle_act(double z, int act, double alpha)
 }
 
 /* One GEMM output element: the K-term dot product, then the bias. */
-static double gemm_z(const uint16_t *A, const uint16_t *B, int dtype, const float *bias,
+static double gemm_z(const void *A, const void *B, int dtype, const float *bias,
                      int64_t N, int64_t K, int64_t i, int64_t j)
 {
     double s = 0.0;
     for (int64_t t = 0; t < K; ++t)
-        s += decode(A[i * K + t], dtype) * decode(B[t * N + j], dtype);
+        s += in_value(A, dtype, i * K + t) * in_value(B, dtype, t * N + j);
     return s + (bias ? (double)bias[j] : 0.0);
 }
 
 /*
- * A: [M,K] row-major codes; B: [K,N] row-major codes; bias: [N] fp32 or NULL;
+ * A: [M,K] row-major; B: [K,N] row-major (16-bit codes of dtype, or fp32
+ * values when dtype == OR_F32); bias: [N] fp32 or NULL;
  * R: residual [M,N] of dtype rdtype (OR_F16 / OR_BF16 codes, OR_F32 floats) or NULL.
  * points == NULL: out[i*N + j] for every element.  Otherwise out[p] is the
  * element at flat index points[p] (= i*N + j).  Returns 0, or -1 on a bad
  * argument.
  */
-int oracle_gemm_res(const uint16_t *A, const uint16_t *B, int dtype, const float *bias,
+int oracle_gemm_res(const void *A, const void *B, int dtype, const float *bias,
                     const void *R, int rdtype, int64_t M, int64_t N, int64_t K, int act,
                     double alpha, const int64_t *points, int64_t npoints, double *out)
 {
-    if (M < 0 || N < 0 || K < 0 || (dtype != OR_F16 && dtype != OR_BF16)) return -1;
-    if (R != NULL && rdtype != OR_F16 && rdtype != OR_BF16 && rdtype != OR_F32) return -1;
+    if (M < 0 || N < 0 || K < 0 || !valid_in_dtype(dtype)) return -1;
+    if (R != NULL && !valid_in_dtype(rdtype)) return -1;
     int64_t count = points ? npoints : M * N;
     for (int64_t p = 0; p < count; ++p) {
         int64_t idx = points ? points[p] : p;
@@ -193,7 +209,7 @@ int oracle_gemm_res(const uint16_t *A, const uint16_t *B, int dtype, const float
 }
 
 /* As oracle_gemm_res with no residual. */
-int oracle_gemm(const uint16_t *A, const uint16_t *B, int dtype, const float *bias,
+int oracle_gemm(const void *A, const void *B, int dtype, const float *bias,
                 int64_t M, int64_t N, int64_t K, int act, double alpha,
                 const int64_t *points, int64_t npoints, double *out)
 {
@@ -215,7 +231,7 @@ typedef struct {
 } conv_geom;
 
 /* One conv output element, by direct summation over (ci, r, q). */
-static double conv_z(const uint16_t *x, const uint16_t *w, int dtype, const float *bias,
+static double conv_z(const void *x, const void *w, int dtype, const float *bias,
                      const conv_geom *g, int64_t n, int64_t co, int64_t oh, int64_t ow)
 {
     double s = 0.0;
@@ -225,28 +241,29 @@ static double conv_z(const uint16_t *x, const uint16_t *w, int dtype, const floa
                 int64_t ih = oh * g->sh - g->pt + r * g->dh;
                 int64_t iw = ow * g->sw - g->pl + q * g->dw;
                 if (ih < 0 || ih >= g->H || iw < 0 || iw >= g->W) continue;  /* zero padding */
-                double xv = decode(x[((n * g->C + ci) * g->H + ih) * g->W + iw], dtype);
-                double wv = decode(w[((co * g->C + ci) * g->kh + r) * g->kw + q], dtype);
+                double xv = in_value(x, dtype, ((n * g->C + ci) * g->H + ih) * g->W + iw);
+                double wv = in_value(w, dtype, ((co * g->C + ci) * g->kh + r) * g->kw + q);
                 s += wv * xv;
             }
     return s + (bias ? (double)bias[co] : 0.0);
 }
 
 /*
- * x: [Nb,C,H,W] codes; w: [Co,C,kh,kw] codes; bias: [Co] fp32 or NULL;
+ * x: [Nb,C,H,W]; w: [Co,C,kh,kw] (16-bit codes of dtype, or fp32 values
+ * when dtype == OR_F32); bias: [Co] fp32 or NULL;
  * R: residual [Nb,Co,Ho,Wo] of dtype rdtype, or NULL.
  * pads = (top, bottom, left, right).  y is [Nb,Co,Ho,Wo]; points are flat
  * indices into y (NULL = all).  Returns 0, or -1 on a bad argument.
  */
-int oracle_conv2d_res(const uint16_t *x, const uint16_t *w, int dtype, const float *bias,
+int oracle_conv2d_res(const void *x, const void *w, int dtype, const float *bias,
                       const void *R, int rdtype,
                       int64_t Nb, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
                       int64_t sh, int64_t sw, int64_t pt, int64_t pb, int64_t pl, int64_t pr,
                       int64_t dh, int64_t dw, int act, double alpha,
                       const int64_t *points, int64_t npoints, double *out)
 {
-    if (dtype != OR_F16 && dtype != OR_BF16) return -1;
-    if (R != NULL && rdtype != OR_F16 && rdtype != OR_BF16 && rdtype != OR_F32) return -1;
+    if (!valid_in_dtype(dtype)) return -1;
+    if (R != NULL && !valid_in_dtype(rdtype)) return -1;
     if (Nb < 0 || C < 0 || H < 0 || W < 0 || Co < 0 || kh <= 0 || kw <= 0) return -1;
     if (pt < 0 || pb < 0 || pl < 0 || pr < 0) return -1;
     conv_geom g = {Nb, C, H, W, Co, kh, kw, sh, sw, pt, pb, pl, pr, dh, dw, 0, 0};
@@ -269,7 +286,7 @@ int oracle_conv2d_res(const uint16_t *x, const uint16_t *w, int dtype, const flo
 }
 
 /* As oracle_conv2d_res with no residual. */
-int oracle_conv2d(const uint16_t *x, const uint16_t *w, int dtype, const float *bias,
+int oracle_conv2d(const void *x, const void *w, int dtype, const float *bias,
                   int64_t Nb, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
                   int64_t sh, int64_t sw, int64_t pt, int64_t pb, int64_t pl, int64_t pr,
                   int64_t dh, int64_t dw, int act, double alpha,

@@ -274,6 +274,23 @@ def check_gemm_residual_golden(orc):
     assert np.array_equal(got, np.asarray(g["expected"]))
 
 
+def check_gemm_f32_inputs(orc):
+    # fp32 inputs are used exactly: brute force against torch float64 of the same values,
+    # and identity B copies A
+    rng = np.random.default_rng(16)
+    for (M, N, K) in ((3, 5, 7), (6, 2, 9)):
+        A = rng.uniform(-2, 2, (M, K)).astype(np.float32)
+        B = rng.uniform(-2, 2, (K, N)).astype(np.float32)
+        bias = rng.uniform(-1, 1, N).astype(np.float32)
+        z = (torch.from_numpy(A.astype(np.float64)) @ torch.from_numpy(B.astype(np.float64))).numpy()
+        exp = act_ref(z + bias.astype(np.float64)[None, :], "leaky_relu", 0.1)
+        got = orc.gemm(A, B, "f32", bias, "leaky_relu", 0.1)
+        assert np.allclose(got, exp, rtol=1e-13, atol=1e-13)
+    A = np.float32([[1.0 + 2.0 ** -20, -3.25], [0.1, 7.0]])       # not representable in 16 bits
+    got = orc.gemm(A, np.eye(2, dtype=np.float32), "f32", None, "none")
+    assert np.array_equal(got, A.astype(np.float64))
+
+
 # -------------------------------------------------------------------- conv --
 def check_conv_shape(orc):
     # the workloads' own shapes
@@ -300,8 +317,12 @@ def check_conv_shape(orc):
 
 
 def _torch_conv(orc, x, w, dtype, bias, stride, pads, dil):
-    xt = torch.from_numpy(orc.decode(x, dtype))
-    wt = torch.from_numpy(orc.decode(w, dtype))
+    if dtype == "f32":
+        xt = torch.from_numpy(np.asarray(x, dtype=np.float32).astype(np.float64))
+        wt = torch.from_numpy(np.asarray(w, dtype=np.float32).astype(np.float64))
+    else:
+        xt = torch.from_numpy(orc.decode(x, dtype))
+        wt = torch.from_numpy(orc.decode(w, dtype))
     pt, pb, pl, pr = pads
     xt = F.pad(xt, (pl, pr, pt, pb))
     bt = None if bias is None else torch.from_numpy(bias.astype(np.float64))
@@ -417,6 +438,17 @@ def check_conv_golden(orc):
         assert np.allclose(y, exp, rtol=4e-15, atol=1e-15), name
 
 
+def check_conv_f32_inputs(orc):
+    rng = np.random.default_rng(26)
+    x = rng.uniform(-2, 2, (2, 3, 7, 6)).astype(np.float32)
+    w = rng.uniform(-1, 1, (4, 3, 3, 2)).astype(np.float32)
+    bias = rng.uniform(-1, 1, 4).astype(np.float32)
+    for stride, pads, dil in (((1, 1), (1, 1, 1, 1), (1, 1)), ((2, 1), (0, 2, 1, 0), (1, 2))):
+        got = orc.conv2d(x, w, "f32", bias, stride, pads, dil, "none")
+        ref = _torch_conv(orc, x, w, "f32", bias, stride, pads, dil)
+        assert np.allclose(got, ref, rtol=1e-13, atol=1e-13)
+
+
 def check_conv_residual(orc):
     # with no activation the residual enters linearly, element by element in y's own order
     rng = np.random.default_rng(25)
@@ -437,6 +469,7 @@ ALL_CHECKS = [
     check_decode_f16, check_decode_bf16, check_act_points, check_tanh, check_sigmoid, check_gelu,
     check_gemm_identity, check_gemm_permutation, check_gemm_ones, check_gemm_bruteforce,
     check_gemm_points, check_gemm_golden, check_gemm_residual_identity, check_gemm_residual_golden,
+    check_gemm_f32_inputs,
     check_conv_shape, check_conv_bruteforce, check_conv_delta, check_conv_as_gemm,
-    check_conv_points, check_conv_golden, check_conv_residual,
+    check_conv_points, check_conv_golden, check_conv_residual, check_conv_f32_inputs,
 ]

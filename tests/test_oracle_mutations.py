@@ -17,7 +17,7 @@ SRC = oracle.SOURCE
 
 MUTANTS = {
     "bias dropped": ("return s + (bias ? (double)bias[j] : 0.0);", "return s;"),
-    "B read transposed": ("B[t * N + j]", "B[j * K + t]"),
+    "B read transposed": ("in_value(B, dtype, t * N + j)", "in_value(B, dtype, j * K + t)"),
     "K loop short by one": ("for (int64_t t = 0; t < K; ++t)", "for (int64_t t = 0; t + 1 < K; ++t)"),
     "leaky slope sign": ("z > 0.0 ? z : alpha * z", "z > 0.0 ? z : -alpha * z"),
     "relu passes negatives": ("z > 0.0 ? z : 0.0", "z > 0.0 ? z : 0.5 * z"),
@@ -40,8 +40,9 @@ MUTANTS = {
     "residual dropped": ("return R ? z + residual_value(R, rdtype, idx) : z;", "return z;"),
     "residual after the activation": ("oracle_act(add_residual(z, R, rdtype, idx), act, alpha)",
                                       "add_residual(oracle_act(z, act, alpha), R, rdtype, idx)"),
-    "residual codes read as bf16": ("return decode(((const uint16_t *)R)[idx], rdtype);",
-                                    "return decode(((const uint16_t *)R)[idx], OR_BF16);"),
+    "residual codes read as bf16": ("return in_value(R, rdtype, idx);", "return in_value(R, OR_BF16, idx);"),
+    "fp32 inputs narrowed": ("if (dtype == OR_F32) return (double)((const float *)p)[idx];",
+                             "if (dtype == OR_F32) return (double)(_Float16)((const float *)p)[idx];"),
     "f16 exponent bias": ("e - 15)", "e - 14)"),
     "f16 subnormal scale": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
     "bf16 fraction width": ("(double)f / 128.0", "(double)f / 256.0"),
