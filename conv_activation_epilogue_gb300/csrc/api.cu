@@ -233,10 +233,11 @@ mmact_status conv_geom(int64_t H, int64_t W, int64_t kh, int64_t kw, const int32
 mmact_status conv_check(const void *x, const void *w, const float *bias, const void *y, int64_t N,
                         int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
                         const int32_t *st, const int32_t *pd, const int32_t *dl, mmact_dtype in,
-                        mmact_dtype out, mmact_act act, ConvGeom *g)
+                        mmact_dtype out, mmact_act act, ConvGeom *g, bool f32_in = false)
 {
     if (N < 0 || C < 0 || Co < 0) return MMACT_ERR_INVALID_ARG;
-    if (!valid_in(in) || !valid_out(out) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
+    const bool in_ok = valid_in(in) || (f32_in && in == MMACT_F32);
+    if (!in_ok || !valid_out(out) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
     mmact_status s = conv_geom(H, W, kh, kw, st, pd, dl, g);
     if (s != MMACT_OK) return s;
     // a pointer may be null only when its tensor is empty
@@ -427,7 +428,10 @@ mmact_status nhwc_enqueue(const void *x, const void *w, const float *bias, void 
     a.Ho = (int)g.Ho;
     a.Wo = (int)g.Wo;
     a.M = (int)M;
-    a.ncb = (int)((C + 63) / 64);
+    a.tf32 = in == MMACT_F32 ? 1 : 0;
+    const int ie = elem_bytes(in);              // 2, or 4 for fp32 inputs
+    a.kc = 128 / ie;                            // one 128-byte row of K per block
+    a.ncb = (int)((C + a.kc - 1) / a.kc);
     // M tile: TH output rows x TW output columns of one image, 128 pixels
     a.TW = g.Wo <= 32 ? 32 : 64;
     if (a.TW * a.sw > 256) a.TW = 32;
@@ -458,7 +462,7 @@ mmact_status nhwc_enqueue(const void *x, const void *w, const float *bias, void 
     a.ab_bf16 = in == MMACT_BF16 ? 1 : 0;
     a.act = (int)act;
     a.alpha = alpha;
-    a.x = static_cast<const uint16_t *>(x);
+    a.x = x;
     a.bias = bias;
     a.status = dev->status;
     a.wait_ns = g_wait_ns.load();
@@ -466,12 +470,12 @@ mmact_status nhwc_enqueue(const void *x, const void *w, const float *bias, void 
     L.out = out_kind(out);
     L.grid = (int)std::min<int64_t>(a.num_tiles, dev->sm_count);
     const uint64_t dX[4] = {(uint64_t)C, (uint64_t)W, (uint64_t)H, (uint64_t)N};
-    const uint64_t sX[3] = {(uint64_t)C * 2, (uint64_t)W * C * 2, (uint64_t)H * W * C * 2};
-    const uint32_t bX[4] = {64, (uint32_t)(a.TW * a.sw), (uint32_t)(a.TH * a.sh), 1};
+    const uint64_t sX[3] = {(uint64_t)C * ie, (uint64_t)W * C * ie, (uint64_t)H * W * C * ie};
+    const uint32_t bX[4] = {(uint32_t)a.kc, (uint32_t)(a.TW * a.sw), (uint32_t)(a.TH * a.sh), 1};
     const uint32_t eX[4] = {1, (uint32_t)a.sw, (uint32_t)a.sh, 1};
     const uint64_t dW[3] = {(uint64_t)C, (uint64_t)(kh * kw), (uint64_t)Co};
-    const uint64_t sW[2] = {(uint64_t)C * 2, (uint64_t)(kh * kw) * C * 2};
-    const uint32_t bW[3] = {64, 1, (uint32_t)bn};
+    const uint64_t sW[2] = {(uint64_t)C * ie, (uint64_t)(kh * kw) * C * ie};
+    const uint32_t bW[3] = {(uint32_t)a.kc, 1, (uint32_t)bn};
     const int e = elem_bytes(out);
     const uint64_t dY[4] = {(uint64_t)Co, (uint64_t)g.Wo, (uint64_t)g.Ho, (uint64_t)N};
     const uint64_t sY[3] = {(uint64_t)Co * e, (uint64_t)g.Wo * Co * e, (uint64_t)g.Ho * g.Wo * Co * e};
@@ -588,9 +592,10 @@ MMACT_EXPORT mmact_status mmact_conv2d_nhwc(const void *x, const void *w, const 
 {
     ConvGeom g;
     mmact_status s = conv_check(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations,
-                                in_dtype, out_dtype, act, &g);
+                                in_dtype, out_dtype, act, &g, true);
     if (s != MMACT_OK) return s;
-    if (C % 8 != 0 || Co % 8 != 0) return MMACT_ERR_UNSUPPORTED;
+    // 16-byte pitches: channel rows of x and w, output rows of y
+    if ((C * elem_bytes(in_dtype)) % 16 != 0 || Co % 8 != 0) return MMACT_ERR_UNSUPPORTED;
     if (N * g.Ho * g.Wo > MAX_DIM) return MMACT_ERR_UNSUPPORTED;
     return nhwc_enqueue(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations, g, in_dtype,
                         out_dtype, act, alpha, static_cast<cudaStream_t>(stream));

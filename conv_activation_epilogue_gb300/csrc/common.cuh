@@ -167,7 +167,9 @@ struct TileN {
 // threads only store and arrive on the full barrier (release); this thread,
 // after acquiring the barrier, issues the one generic-to-async proxy fence
 // that makes the stores visible to the tensor core's operand reads.
-template <int BN, int STAGES, bool B_KMAJOR = false, bool THREAD_FILLED = false>
+// TF32: the operands are fp32 (kind::tf32, 8 K per instruction = 32 bytes,
+// the same K step as the 16-bit kinds; both operands must be K-major).
+template <int BN, int STAGES, bool B_KMAJOR = false, bool THREAD_FILLED = false, bool TF32 = false>
 __device__ void mma_role(const Pipe &pp, uint32_t sA, uint32_t sB, int num_tiles, int num_kb,
                          uint32_t idesc)
 {
@@ -189,7 +191,8 @@ __device__ void mma_role(const Pipe &pp, uint32_t sA, uint32_t sB, int num_tiles
                 const uint64_t ad = ptx::smem_desc(a0 + 32u * k, 16u, 1024u, ptx::SWIZZLE_128B);
                 const uint64_t bd = B_KMAJOR ? ptx::smem_desc(b0 + 32u * k, 16u, 1024u, ptx::SWIZZLE_128B)
                                              : ptx::smem_desc(b0 + 2048u * k, 8192u, 1024u, ptx::SWIZZLE_128B);
-                ptx::mma_f16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                if constexpr (TF32) ptx::mma_tf32(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                else ptx::mma_f16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
             ptx::mma_commit(pp.empty0 + 8 * stage);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }

@@ -66,7 +66,7 @@ __device__ __forceinline__ void nhwc_tile(int t, const NhwcArgs &p, int &n, int 
     n = rr / p.tiles_oh;
 }
 
-template <int BN, int OUT>
+template <int BN, int OUT, bool TF32>
 __global__ void __launch_bounds__(NhwcCfg<BN>::THREADS, 1)
     conv_nhwc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmY, const NhwcArgs p)
@@ -142,9 +142,9 @@ __global__ void __launch_bounds__(NhwcCfg<BN>::THREADS, 1)
                     if (!pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u)) { ok = false; break; }
                     const uint32_t fb = pp.full0 + 8 * stage;
                     ptx::mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-                    ptx::tma_load_4d(sA + stage * Cfg::A_BYTES, &tmX, fb, cb * 64, ix0 + q * p.dw,
+                    ptx::tma_load_4d(sA + stage * Cfg::A_BYTES, &tmX, fb, cb * p.kc, ix0 + q * p.dw,
                                      iy0 + r * p.dh, n);
-                    ptx::tma_load_3d(sB + stage * Cfg::B_BYTES, &tmW, fb, cb * 64, r * p.kw + q, nb * BN);
+                    ptx::tma_load_3d(sB + stage * Cfg::B_BYTES, &tmW, fb, cb * p.kc, r * p.kw + q, nb * BN);
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -161,8 +161,9 @@ __global__ void __launch_bounds__(NhwcCfg<BN>::THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0)
-            mma_role<BN, STAGES, true>(pp, sA, sB, p.num_tiles, p.num_kb,
-                                       ptx::idesc_f16(p.ab_bf16 != 0, false, false, 128, BN));
+            mma_role<BN, STAGES, true, false, TF32>(pp, sA, sB, p.num_tiles, p.num_kb,
+                                                    TF32 ? ptx::idesc_tf32(128, BN)
+                                                         : ptx::idesc_f16(p.ab_bf16 != 0, false, false, 128, BN));
     } else {
         // -------------------------------------------------------- epilogue --
         // TMEM lane quarter qd holds tile pixels 32qd..32qd+31, which lie in
@@ -221,15 +222,22 @@ __global__ void __launch_bounds__(NhwcCfg<BN>::THREADS, 1)
 template <int BN, int OUT>
 static cudaError_t launch_nhwc_t(const NhwcLaunch &L, cudaStream_t stream)
 {
-    return launch_k(conv_nhwc_kernel<BN, OUT>, L.grid, NhwcCfg<BN>::THREADS, NhwcCfg<BN>::SMEM_BYTES,
+    if (L.args.tf32)
+        return launch_k(conv_nhwc_kernel<BN, OUT, true>, L.grid, NhwcCfg<BN>::THREADS,
+                        NhwcCfg<BN>::SMEM_BYTES, stream, L.tmX, L.tmW, L.tmY, L.args);
+    return launch_k(conv_nhwc_kernel<BN, OUT, false>, L.grid, NhwcCfg<BN>::THREADS, NhwcCfg<BN>::SMEM_BYTES,
                     stream, L.tmX, L.tmW, L.tmY, L.args);
 }
 
 template <int BN, int OUT>
 static cudaError_t setup_nhwc_t()
 {
-    return cudaFuncSetAttribute(conv_nhwc_kernel<BN, OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                NhwcCfg<BN>::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(conv_nhwc_kernel<BN, OUT, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, NhwcCfg<BN>::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(conv_nhwc_kernel<BN, OUT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 NhwcCfg<BN>::SMEM_BYTES);
+    return e;
 }
 
 cudaError_t setup_nhwc_kernels()

@@ -78,7 +78,9 @@ struct NhwcArgs {
     int sh, sw, pt, pl, dh, dw;
     int Ho, Wo;
     int M;               // Nb * Ho * Wo output pixels
-    int ncb;             // channel blocks of 64 per tap
+    int ncb;             // channel blocks of kc per tap
+    int kc;              // channels per K block: 64 (16-bit inputs) or 32 (fp32 inputs): 128 bytes
+    int tf32;            // 1: fp32 inputs, tcgen05 kind::tf32
     int TW, TH;          // output pixels per tile: TH rows x TW columns (TW * TH = 128)
     int tiles_oh, tiles_ow;
     int tiles_m, tiles_n, num_tiles, num_kb;   // tiles_m = Nb * tiles_oh * tiles_ow; num_kb = kh * kw * ncb
@@ -86,7 +88,7 @@ struct NhwcArgs {
     int ab_bf16;
     int act;
     float alpha;
-    const uint16_t *x;
+    const void *x;
     const float *bias;   // [Co] or null
     unsigned int *status;
     unsigned long long wait_ns;

@@ -252,10 +252,11 @@ def mmact_conv2d_split(x, w, bias, y, workspace, stride=(1, 1), pads=(0, 0, 0, 0
 
 def mmact_conv2d_nhwc(x, w, bias, y, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1),
                       act: str = "tanh", alpha: float = 0.0, stream=None) -> None:
-    """Channels-last y = act(conv2d(x, w) + bias): x [N,H,W,C], w [Co,kh,kw,C], y [N,Ho,Wo,Co]."""
+    """Channels-last y = act(conv2d(x, w) + bias): x [N,H,W,C], w [Co,kh,kw,C], y [N,Ho,Wo,Co].
+    x and w may be fp32 (tf32 tensor-core arithmetic, see include/mmact.h)."""
     L = load()
-    px = _dev(x, "x", _IN)
-    pw = _dev(w, "w", _IN)
+    px = _dev(x, "x", _OUT)
+    pw = _dev(w, "w", _OUT)
     py = _dev(y, "y", _OUT)
     if x.dim() != 4 or w.dim() != 4 or y.dim() != 4:
         raise ValueError("x, w, y must be 4-D (NHWC / [Co,kh,kw,C] / NHWC)")

@@ -200,14 +200,17 @@ mmact_status mmact_gemm_split_noalloc(const void *A, const void *B, const float 
  * Channels-last fused conv2d + bias + activation (the layout-converting
  * member of the fused_matmul_relu article's fusion families applied to the
  * Fused ConvTanh operator):  y = act(conv2d(x, w) + bias).
- *   x    [N, H, W, C] in_dtype (F16 or BF16), channels innermost (NHWC)
+ *   x    [N, H, W, C] in_dtype (F16, BF16 or F32), channels innermost (NHWC)
  *   w    [Co, kh, kw, C] in_dtype, channels innermost
  *   bias [Co] fp32, or NULL
  *   y    [N, Ho, Wo, Co] out_dtype (F32, F16 or BF16), NHWC; fully overwritten
- * strides / pads / dilations and Ho, Wo as for mmact_conv2d.  Requires
- * C % 8 == 0 and Co % 8 == 0 (16-byte channel vectors and rows), else
- * MMACT_ERR_UNSUPPORTED.  N == 0 or Co == 0 enqueues nothing; C == 0 gives
- * y = act(bias).
+ * strides / pads / dilations and Ho, Wo as for mmact_conv2d.  F32 inputs
+ * (the Fused ConvTanh article evaluates fp32 cases beside fp16 and bf16) run
+ * on the tensor cores as tf32: each operand keeps 10 fraction bits, so
+ * |error| <= about 2^-9 * sum_k |x_k w_k| beyond the fp32 accumulation.
+ * Requires C * sizeof(in_dtype) % 16 == 0 and Co % 8 == 0 (16-byte channel
+ * rows), else MMACT_ERR_UNSUPPORTED.  N == 0 or Co == 0 enqueues nothing;
+ * C == 0 gives y = act(bias).
  */
 mmact_status mmact_conv2d_nhwc(const void *x, const void *w, const float *bias, void *y,
                                int64_t N, int64_t C, int64_t H, int64_t W,
