@@ -186,11 +186,18 @@ def workload_bytes(mmact, wl):
 class NhwcProblem:
     """A conv workload in channels-last layout (same values, transposed on the host)."""
 
-    def __init__(self, torch, mmact, wl, device, inputs=None):
+    def __init__(self, torch, mmact, wl, device, inputs=None, fp32_inputs=False):
         self.mmact, self.wl = mmact, wl
         inp = inputs if inputs is not None else wl.inputs()
-        self.x = codes_to(torch, np.ascontiguousarray(inp["x"].transpose(0, 2, 3, 1)), wl.dtype, device)
-        self.w = codes_to(torch, np.ascontiguousarray(inp["w"].transpose(0, 2, 3, 1)), wl.dtype, device)
+        x = np.ascontiguousarray(inp["x"].transpose(0, 2, 3, 1))
+        w = np.ascontiguousarray(inp["w"].transpose(0, 2, 3, 1))
+        if fp32_inputs:
+            # the same values widened to fp32 (exact); the kernel runs them as tf32
+            self.x = codes_to(torch, x, wl.dtype, device).float()
+            self.w = codes_to(torch, w, wl.dtype, device).float()
+        else:
+            self.x = codes_to(torch, x, wl.dtype, device)
+            self.w = codes_to(torch, w, wl.dtype, device)
         self.bias = torch.from_numpy(inp["bias"]).to(device)
         Ho, Wo = mmact.mmact_conv2d_out_shape(wl.H, wl.W, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation)
         self.out = torch.empty((wl.N, Ho, Wo, wl.Co), dtype=torch_dtype(torch, wl.out_dtype), device=device)
@@ -233,6 +240,10 @@ class Problem:
         if wl.kind == "gemm":
             if variant == "fused":
                 m.mmact_gemm(self.A, self.B, self.bias, self.out, wl.act, wl.alpha, stream)
+            elif variant == "fused_residual":
+                if getattr(self, "res", None) is None:
+                    self.res = self.torch.ones_like(self.out)
+                m.mmact_gemm_residual(self.A, self.B, self.bias, self.res, self.out, wl.act, wl.alpha, stream)
             else:
                 m.mmact_gemm_split(self.A, self.B, self.bias, self.out, self.workspace(), wl.act,
                                    wl.alpha, stream)
@@ -573,12 +584,20 @@ def sweep(torch, mmact, device, stream, peaks):
         flops = workload_flops(mmact, wl)
         nbytes = workload_bytes(mmact, wl)
         rec = {"timing": "CUDA graph of 20 back-to-back calls, replayed 3 times"}
-        for variant in ("fused", "split"):
+        variants = ("fused", "split") + (("fused_residual",) if wl.kind == "gemm" else ())
+        for variant in variants:
             ms = time_graph(torch, lambda: prob.run(variant), 20, stream)
             tf = flops / (ms * 1e-3) / 1e12
+            nb = nbytes + (prob.out.numel() * prob.out.element_size() if variant == "fused_residual" else 0)
             rec[variant] = {"ms": round(ms, 5), "tflops": round(tf, 2),
                             "pct_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 2),
-                            "alg_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+                            "alg_gbs": round(nb / (ms * 1e-3) / 1e9, 1)}
+        # the fused-vs-split decision, re-measured on every run
+        rec["fused_speedup_over_split"] = round(rec["split"]["ms"] / rec["fused"]["ms"], 3)
+        if wl.kind == "conv":
+            rec["nchw_producer"] = mmact.mmact_conv2d_producer(
+                wl.N, wl.C, wl.H, wl.W, wl.Co, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation,
+                torch_dtype(torch, wl.dtype), torch_dtype(torch, wl.out_dtype))
         if wl.kind == "conv":
             # the same convolution on channels-last tensors (x NHWC, w [Co,kh,kw,C], y NHWC)
             nprob = NhwcProblem(torch, mmact, wl, device, inputs=prob.host)
@@ -588,6 +607,13 @@ def sweep(torch, mmact, device, stream, peaks):
                                  "pct_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 2),
                                  "alg_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
             del nprob
+            # fp32 inputs (same values), tf32 tensor-core arithmetic; peak: nominal tf32 = bf16 / 2
+            fprob = NhwcProblem(torch, mmact, wl, device, inputs=prob.host, fp32_inputs=True)
+            ms = time_graph(torch, lambda: fprob.run(), 20, stream)
+            tf = flops / (ms * 1e-3) / 1e12
+            rec["fused_nhwc_fp32_inputs"] = {"ms": round(ms, 5), "tflops": round(tf, 2),
+                                             "pct_tf32_peak": round(200 * tf / peaks["bf16_tflops"], 2)}
+            del fprob
         st = mmact.mmact_get_last_error()
         rec["status"] = mmact.mmact_status_string(st)
         out[wl.name] = rec
