@@ -181,8 +181,18 @@ __global__ void __launch_bounds__(192, 1)
             ptx::tc_fence_after();
             const uint32_t tbase = pp.tmem + ((uint32_t)(q * 32) << 16) + acc * TileN<BN>::ACC_STRIDE;
             const int row0 = mb * 128 + q * 32;
+            if (p.res != nullptr) {
+                // this lane's residual row segment of the first unit (one 128-byte line)
+                const void *r0 = residual_row<OUT>(p, row0 + lane, n0);
+                if (r0 != nullptr) ptx::prefetch_l1(r0);
+            }
 #pragma unroll 1
             for (int u = 0; u < BN / COLS; ++u) {
+                if (p.res != nullptr && u + 1 < BN / COLS + (BN % COLS != 0 ? 1 : 0)) {
+                    // the next unit's segment, fetched while this unit runs
+                    const void *rn = residual_row<OUT>(p, row0 + lane, n0 + (u + 1) * COLS);
+                    if (rn != nullptr && n0 + (u + 1) * COLS < p.N) ptx::prefetch_l1(rn);
+                }
                 const uint32_t buf = my_buf + (units++ & 1u) * 4096u;
                 if (lane == 0) ptx::bulk_wait_read<1>();   // the store that last used `buf` has read it
                 __syncwarp();

@@ -29,6 +29,12 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
+// Non-binding prefetch of the cache line holding `p` into L1.
+__device__ __forceinline__ void prefetch_l1(const void *p)
+{
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // ----------------------------------------------- programmatic dependent launch --
 // Lets the next kernel in the stream be scheduled now (its blocks still wait
 // in griddep_wait until this grid has finished).  No effect when the launch
