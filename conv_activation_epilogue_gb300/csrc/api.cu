@@ -337,7 +337,7 @@ mmact_status conv_enqueue(const void *x, const void *w, const float *bias, void 
                           int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
                           const int32_t *st, const int32_t *pd, const int32_t *dl, const ConvGeom &g,
                           mmact_dtype in, mmact_dtype out, mmact_act act, float alpha,
-                          cudaStream_t stream)
+                          cudaStream_t stream, const void *res = nullptr)
 {
     DeviceInfo *dev = nullptr;
     mmact_status s = device_info(&dev);
@@ -345,7 +345,8 @@ mmact_status conv_enqueue(const void *x, const void *w, const float *bias, void 
     const int64_t P = g.Ho * g.Wo;
     if (N == 0 || Co == 0 || P == 0) return MMACT_OK;
     if (C == 0) {
-        cudaError_t e = launch_bias_act(bias, y, N * Co, P, 1, Co, out_kind(out), (int)act, alpha, stream);
+        cudaError_t e = launch_bias_act(bias, y, N * Co, P, 1, Co, out_kind(out), (int)act, alpha, stream,
+                                        res);
         return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
     }
     ConvLaunch L;
@@ -357,6 +358,7 @@ mmact_status conv_enqueue(const void *x, const void *w, const float *bias, void 
     a.x = static_cast<const uint16_t *>(x);
     a.w = static_cast<const uint16_t *>(w);
     a.bias = bias;
+    a.res = res;
     a.y = y;
     a.status = dev->status;
     a.wait_ns = g_wait_ns.load();
@@ -398,7 +400,7 @@ mmact_status nhwc_enqueue(const void *x, const void *w, const float *bias, void 
                           int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
                           const int32_t *st, const int32_t *pd, const int32_t *dl, const ConvGeom &g,
                           mmact_dtype in, mmact_dtype out, mmact_act act, float alpha,
-                          cudaStream_t stream)
+                          cudaStream_t stream, const void *res = nullptr)
 {
     DeviceInfo *dev = nullptr;
     mmact_status s = device_info(&dev);
@@ -406,7 +408,7 @@ mmact_status nhwc_enqueue(const void *x, const void *w, const float *bias, void 
     const int64_t M = N * g.Ho * g.Wo;
     if (M == 0 || Co == 0) return MMACT_OK;
     if (C == 0) {
-        cudaError_t e = launch_bias_act(bias, y, M, Co, 0, Co, out_kind(out), (int)act, alpha, stream);
+        cudaError_t e = launch_bias_act(bias, y, M, Co, 0, Co, out_kind(out), (int)act, alpha, stream, res);
         return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
     }
     NhwcLaunch L;
@@ -464,6 +466,7 @@ mmact_status nhwc_enqueue(const void *x, const void *w, const float *bias, void 
     a.alpha = alpha;
     a.x = x;
     a.bias = bias;
+    a.res = res;
     a.status = dev->status;
     a.wait_ns = g_wait_ns.load();
     L.tile_n = bn;
@@ -484,6 +487,17 @@ mmact_status nhwc_enqueue(const void *x, const void *w, const float *bias, void 
         !encode(&L.tmY, out, 4, y, dY, sY, bY))
         return MMACT_ERR_CUDA;
     return launch_conv_nhwc(L, stream) == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
+}
+
+// R is read element by element before the same element of the output is
+// written, so R == out is allowed; any other overlap is not.
+mmact_status residual_check(const void *R, const void *out, int64_t bytes)
+{
+    if (R == nullptr && bytes != 0) return MMACT_ERR_INVALID_ARG;
+    if (!aligned16(R)) return MMACT_ERR_UNSUPPORTED;
+    const char *r = static_cast<const char *>(R), *c = static_cast<const char *>(out);
+    if (r != c && bytes != 0 && r < c + bytes && c < r + bytes) return MMACT_ERR_INVALID_ARG;
+    return MMACT_OK;
 }
 
 }  // namespace
@@ -555,6 +569,44 @@ MMACT_EXPORT mmact_status mmact_conv2d(const void *x, const void *w, const float
     if (s != MMACT_OK) return s;
     return conv_enqueue(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations, g, in_dtype,
                         out_dtype, act, alpha, static_cast<cudaStream_t>(stream));
+}
+
+MMACT_EXPORT mmact_status mmact_conv2d_residual(const void *x, const void *w, const float *bias,
+                                                const void *R, void *y, int64_t N, int64_t C, int64_t H,
+                                                int64_t W, int64_t Co, int64_t kh, int64_t kw,
+                                                const int32_t strides[2], const int32_t pads[4],
+                                                const int32_t dilations[2], mmact_dtype in_dtype,
+                                                mmact_dtype out_dtype, mmact_act act, float alpha,
+                                                void *stream)
+{
+    ConvGeom g;
+    mmact_status s = conv_check(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations,
+                                in_dtype, out_dtype, act, &g);
+    if (s != MMACT_OK) return s;
+    s = residual_check(R, y, N * Co * g.Ho * g.Wo * elem_bytes(out_dtype));
+    if (s != MMACT_OK) return s;
+    return conv_enqueue(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations, g, in_dtype,
+                        out_dtype, act, alpha, static_cast<cudaStream_t>(stream), R);
+}
+
+MMACT_EXPORT mmact_status mmact_conv2d_nhwc_residual(const void *x, const void *w, const float *bias,
+                                                     const void *R, void *y, int64_t N, int64_t C,
+                                                     int64_t H, int64_t W, int64_t Co, int64_t kh,
+                                                     int64_t kw, const int32_t strides[2],
+                                                     const int32_t pads[4], const int32_t dilations[2],
+                                                     mmact_dtype in_dtype, mmact_dtype out_dtype,
+                                                     mmact_act act, float alpha, void *stream)
+{
+    ConvGeom g;
+    mmact_status s = conv_check(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations,
+                                in_dtype, out_dtype, act, &g, true);
+    if (s != MMACT_OK) return s;
+    if ((C * elem_bytes(in_dtype)) % 16 != 0 || Co % 8 != 0) return MMACT_ERR_UNSUPPORTED;
+    if (N * g.Ho * g.Wo > MAX_DIM) return MMACT_ERR_UNSUPPORTED;
+    s = residual_check(R, y, N * Co * g.Ho * g.Wo * elem_bytes(out_dtype));
+    if (s != MMACT_OK) return s;
+    return nhwc_enqueue(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations, g, in_dtype,
+                        out_dtype, act, alpha, static_cast<cudaStream_t>(stream), R);
 }
 
 MMACT_EXPORT mmact_status mmact_conv2d_split(const void *x, const void *w, const float *bias,

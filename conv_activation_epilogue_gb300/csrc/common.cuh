@@ -220,20 +220,75 @@ __device__ __forceinline__ float2 unpack2(uint32_t w)
     }
 }
 
-// Adds this lane's residual row segment -- COLS consecutive elements of the
-// output dtype starting at `res` -- to v[0..min(nvalid, COLS)).  Plain,
+// PER residual values of this lane's row segment starting at column c0 (the
+// segment holds elements of the output dtype; columns at or past nvalid read
+// as 0).  One 16-byte load when the chunk is whole and aligned.  Plain,
 // coherent loads (not the read-only path): the residual may be the output
 // tensor itself, each element read here before this unit's store writes it.
+template <int OUT, int PER>
+__device__ __forceinline__ void residual_chunk(const void *res, int nvalid, int c0, float (&v)[PER])
+{
+    constexpr int ESZ = OUT == OUT_F32 ? 4 : 2;
+    static_assert(PER * ESZ == 16, "one chunk is 16 bytes");
+    if (res == nullptr) {                              // this lane's row is out of range
+#pragma unroll
+        for (int j = 0; j < PER; ++j) v[j] = 0.0f;
+        return;
+    }
+    const char *p = static_cast<const char *>(res) + c0 * ESZ;
+    if (c0 + PER <= nvalid && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if constexpr (OUT == OUT_F32) {
+                v[e] = __uint_as_float(w[e]);
+            } else {
+                const float2 f = unpack2<OUT>(w[e]);
+                v[2 * e] = f.x;
+                v[2 * e + 1] = f.y;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            float x = 0.0f;
+            if (c0 + j < nvalid) {
+                if constexpr (OUT == OUT_F32) x = reinterpret_cast<const float *>(p)[j];
+                else if constexpr (OUT == OUT_BF16) x = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[j]);
+                else x = __half2float(reinterpret_cast<const __half *>(p)[j]);
+            }
+            v[j] = x;
+        }
+    }
+}
+
+// a + r when the residual is read in the packing loop, a otherwise (no add:
+// a + 0.0f is not an identity in IEEE arithmetic, -0 + 0 = +0).
+template <bool ADD>
+__device__ __forceinline__ float plus_if(float a, float r)
+{
+    if constexpr (ADD) return a + r;
+    else return a;
+}
+
+// Adds this lane's residual row segment -- COLS elements of the output dtype
+// from `res` -- to v[0..min(nvalid, COLS)): one branch, then all of its
+// 16-byte loads issued together (coherent loads: the residual may be the
+// output tensor itself, each element read before this unit's store).
 template <int OUT, int COLS>
 __device__ __forceinline__ void add_residual(const void *res, int nvalid, float (&v)[COLS])
 {
-    if (nvalid >= COLS) {
+    constexpr int PER = OUT == OUT_F32 ? 4 : 8;      // elements per 16 bytes
+    if (res == nullptr) return;                        // this lane's row is out of range
+    if (nvalid >= COLS && (reinterpret_cast<uintptr_t>(res) & 15u) == 0) {
         const uint4 *q = reinterpret_cast<const uint4 *>(res);
-        constexpr int PER = OUT == OUT_F32 ? 4 : 8;      // elements per 16 bytes
+        uint4 u[COLS / PER];
+#pragma unroll
+        for (int c = 0; c < COLS / PER; ++c) u[c] = q[c];
 #pragma unroll
         for (int c = 0; c < COLS / PER; ++c) {
-            const uint4 u = q[c];
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 if constexpr (OUT == OUT_F32) {
@@ -247,13 +302,11 @@ __device__ __forceinline__ void add_residual(const void *res, int nvalid, float 
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < COLS; ++j) {
-            if (j < nvalid) {
-                if constexpr (OUT == OUT_F32) v[j] += static_cast<const float *>(res)[j];
-                else if constexpr (OUT == OUT_BF16)
-                    v[j] += __bfloat162float(static_cast<const __nv_bfloat16 *>(res)[j]);
-                else v[j] += __half2float(static_cast<const __half *>(res)[j]);
-            }
+        for (int c = 0; c < COLS; c += PER) {
+            float rv[PER];
+            residual_chunk<OUT, PER>(res, nvalid, c, rv);
+#pragma unroll
+            for (int j = 0; j < PER; ++j) v[c + j] += rv[j];
         }
     }
 }
@@ -270,7 +323,7 @@ __device__ __forceinline__ void add_residual(const void *res, int nvalid, float 
 // NCOL = 32 with a 16-bit output is the narrow tail unit of a 224-wide tile:
 // 64-byte rows, written densely without swizzle (its TMA store uses an
 // unswizzled map).
-template <int OUT, int ACT, bool BIAS_ROW, int NCOL = (OUT == OUT_F32 ? 32 : 64)>
+template <int OUT, int ACT, bool BIAS_ROW, int NCOL, bool RES>
 __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, int nvalid,
                                          float brow, float alpha, uint32_t buf, int lane,
                                          const void *res)
@@ -298,7 +351,16 @@ __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, 
         for (int j = 0; j < COLS; ++j)
             bc[j] = BIAS_ROW ? brow : ((bias_col != nullptr && j < nvalid) ? __ldg(bias_col + j) : 0.0f);
     }
-    if (res != nullptr) add_residual<OUT, COLS>(res, nvalid, bc);
+    // Residual.  With a per-column bias (GEMM, channels-last conv) bc[] is a
+    // per-lane array already: the whole row segment is added into it, its
+    // loads issued together before the TMEM wait.  With a per-row bias (NCHW
+    // conv) bc[] folds to one register, so the residual is read chunk by
+    // chunk in the packing loops instead (from L1: the caller prefetches).
+    if constexpr (RES && !BIAS_ROW) {
+        add_residual<OUT, COLS>(res, nvalid, bc);
+        __syncwarp();                                  // converge before the warp-collective wait
+    }
+    constexpr bool CHUNKED = RES && BIAS_ROW;
     ptx::tmem_ld_wait(r0);
     if constexpr (WIDE) ptx::tmem_ld_wait(r1);
     if constexpr (OUT != OUT_F32 && !WIDE) {
@@ -306,12 +368,15 @@ __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, 
         const uint32_t row = buf + (uint32_t)lane * 64u;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+            float rv[8] = {};
+            if constexpr (CHUNKED) residual_chunk<OUT, 8>(res, nvalid, 8 * c, rv);
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int col = 8 * c + 2 * e;
-                w[e] = pack2<OUT>(act_f32<ACT>(__uint_as_float(r0[col]) + bc[col], alpha),
-                                  act_f32<ACT>(__uint_as_float(r0[col + 1]) + bc[col + 1], alpha));
+                w[e] = pack2<OUT>(act_f32<ACT>(plus_if<CHUNKED>(__uint_as_float(r0[col]) + bc[col], rv[2 * e]), alpha),
+                                  act_f32<ACT>(plus_if<CHUNKED>(__uint_as_float(r0[col + 1]) + bc[col + 1], rv[2 * e + 1]),
+                                               alpha));
             }
             ptx::st_shared_v4(row + (uint32_t)c * 16u, w[0], w[1], w[2], w[3]);
         }
@@ -322,11 +387,13 @@ __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, 
     if constexpr (OUT == OUT_F32) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
+            float rv[4] = {};
+            if constexpr (CHUNKED) residual_chunk<OUT, 4>(res, nvalid, 4 * c, rv);
             float v[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int col = 4 * c + e;
-                v[e] = act_f32<ACT>(__uint_as_float(r0[col]) + bc[col], alpha);
+                v[e] = act_f32<ACT>(plus_if<CHUNKED>(__uint_as_float(r0[col]) + bc[col], rv[e]), alpha);
             }
             ptx::st_shared_v4(row + (((uint32_t)c ^ sw) << 4), __float_as_uint(v[0]),
                               __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
@@ -334,45 +401,63 @@ __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, 
     } else {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
+            float rv[8] = {};
+            if constexpr (CHUNKED) residual_chunk<OUT, 8>(res, nvalid, 8 * c, rv);
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int col = 8 * c + 2 * e;
                 const uint32_t ua = col < 32 ? r0[col] : r1[col - 32];
                 const uint32_t ub = col + 1 < 32 ? r0[col + 1] : r1[col + 1 - 32];
-                w[e] = pack2<OUT>(act_f32<ACT>(__uint_as_float(ua) + bc[col], alpha),
-                                  act_f32<ACT>(__uint_as_float(ub) + bc[col + 1], alpha));
+                w[e] = pack2<OUT>(act_f32<ACT>(plus_if<CHUNKED>(__uint_as_float(ua) + bc[col], rv[2 * e]), alpha),
+                                  act_f32<ACT>(plus_if<CHUNKED>(__uint_as_float(ub) + bc[col + 1], rv[2 * e + 1]), alpha));
             }
             ptx::st_shared_v4(row + (((uint32_t)c ^ sw) << 4), w[0], w[1], w[2], w[3]);
         }
     }
 }
 
-template <int OUT, bool BIAS_ROW, int NCOL = (OUT == OUT_F32 ? 32 : 64)>
-__device__ __forceinline__ void epi_unit_dispatch(int act, uint32_t taddr, const float *bias_col,
-                                                  int nvalid, float brow, float alpha, uint32_t buf,
-                                                  int lane, const void *res = nullptr)
+template <int OUT, bool BIAS_ROW, int NCOL, bool RES>
+__device__ __forceinline__ void epi_unit_act(int act, uint32_t taddr, const float *bias_col, int nvalid,
+                                             float brow, float alpha, uint32_t buf, int lane,
+                                             const void *res)
 {
     switch (act) {
     case ACT_RELU:
-        epi_unit<OUT, ACT_RELU, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+        epi_unit<OUT, ACT_RELU, BIAS_ROW, NCOL, RES>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     case ACT_LEAKY:
-        epi_unit<OUT, ACT_LEAKY, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+        epi_unit<OUT, ACT_LEAKY, BIAS_ROW, NCOL, RES>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     case ACT_TANH:
-        epi_unit<OUT, ACT_TANH, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+        epi_unit<OUT, ACT_TANH, BIAS_ROW, NCOL, RES>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     case ACT_SIGMOID:
-        epi_unit<OUT, ACT_SIGMOID, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+        epi_unit<OUT, ACT_SIGMOID, BIAS_ROW, NCOL, RES>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     case ACT_GELU:
-        epi_unit<OUT, ACT_GELU, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+        epi_unit<OUT, ACT_GELU, BIAS_ROW, NCOL, RES>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     default:
-        epi_unit<OUT, ACT_NONE, BIAS_ROW, NCOL>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+        epi_unit<OUT, ACT_NONE, BIAS_ROW, NCOL, RES>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     }
+}
+
+// One epilogue unit with the activation and the presence of a residual
+// resolved once: the residual-free code carries no residual work.  `has_res`
+// must be the same for every lane of the warp (the unit's tcgen05.ld is
+// warp-collective); a lane whose row is out of range passes res == nullptr
+// and adds nothing.
+template <int OUT, bool BIAS_ROW, int NCOL = (OUT == OUT_F32 ? 32 : 64)>
+__device__ __forceinline__ void epi_unit_dispatch(int act, uint32_t taddr, const float *bias_col,
+                                                  int nvalid, float brow, float alpha, uint32_t buf,
+                                                  int lane, const void *res = nullptr, bool has_res = false)
+{
+    if (has_res)
+        epi_unit_act<OUT, BIAS_ROW, NCOL, true>(act, taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+    else
+        epi_unit_act<OUT, BIAS_ROW, NCOL, false>(act, taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
 }
 
 }  // namespace mmact

@@ -236,8 +236,14 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
                 const int pix0 = pb * BN + u * COLS;
                 if (lane == 0) ptx::bulk_wait_read<1>();
                 __syncwarp();
-                epi_unit_dispatch<OUT, true>(p.act, tbase + u * COLS, nullptr, 0, brow, p.alpha, buf,
-                                             lane);
+                const void *rrow = nullptr;      // this lane's channel, pixels pix0.. (contiguous in y)
+                if (p.res != nullptr && co < p.Co && pix0 < p.P) {
+                    rrow = static_cast<const char *>(p.res) +
+                           (((int64_t)n * p.Co + co) * p.P + pix0) * (OUT == OUT_F32 ? 4 : 2);
+                    ptx::prefetch_l1(rrow);
+                }
+                epi_unit_dispatch<OUT, true>(p.act, tbase + u * COLS, nullptr, p.P - pix0, brow, p.alpha, buf,
+                                             lane, rrow, p.res != nullptr);
                 if (p.y_tma) {
                     ptx::fence_proxy_async_smem();
                     __syncwarp();

@@ -189,9 +189,15 @@ __global__ void __launch_bounds__(NhwcCfg<BN>::THREADS, 1)
                 if (lane == 0) ptx::bulk_wait_read<0>();
                 __syncwarp();
                 const int col0 = n0 + u * COLS;
+                const void *rrow = nullptr;      // this lane's pixel: channels col0.. of the residual
+                if (p.res != nullptr && oh < p.Ho && ow + lane < p.Wo) {
+                    constexpr int ESZ = OUT == OUT_F32 ? 4 : 2;
+                    rrow = static_cast<const char *>(p.res) +
+                           ((((int64_t)n * p.Ho + oh) * p.Wo + ow + lane) * p.Co + col0) * ESZ;
+                }
                 epi_unit_dispatch<OUT, false>(p.act, tbase + u * COLS,
                                               p.bias != nullptr ? p.bias + col0 : nullptr, p.Co - col0,
-                                              0.0f, p.alpha, buf, lane);
+                                              0.0f, p.alpha, buf, lane, rrow, p.res != nullptr);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && oh < p.Ho && ow < p.Wo && col0 < p.Co) {

@@ -178,7 +178,35 @@ __global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
     // tbase + u * COLS, staged in `buf` and stored by TMA.
     auto store_unit = [&](int n, int toh, int tow, int co_row0, float brow, uint32_t tbase, int u,
                           uint32_t buf) {
-        epi_unit_dispatch<OUT, true>(p.act, tbase + u * COLS, nullptr, 0, brow, p.alpha, buf, lane);
+        // this lane's channel: the unit's pixels are contiguous in y (one output
+        // row when TW = 64, consecutive pixels of the image when TW = 32)
+        const void *rrow = nullptr;
+        int rvalid = 0;
+        if (p.res != nullptr && co_row0 + lane < p.Co) {
+            constexpr int ESZ = OUT == OUT_F32 ? 4 : 2;
+            const int col = u * COLS;
+            int64_t off = -1;
+            if (p.TW == 32) {
+                const int pix0 = toh * p.TH * p.Wo + col;
+                if (pix0 < p.P) {
+                    off = ((int64_t)n * p.Co + co_row0 + lane) * p.P + pix0;
+                    rvalid = p.P - pix0;
+                }
+            } else {
+                const int oh = toh * p.TH + col / 64, ow = tow * 64 + (col & 63);
+                if (oh < p.Ho && ow < p.Wo) {
+                    off = (((int64_t)n * p.Co + co_row0 + lane) * p.Ho + oh) * p.Wo + ow;
+                    rvalid = p.Wo - ow;
+                }
+            }
+            if (off >= 0) {
+                rrow = static_cast<const char *>(p.res) + off * ESZ;
+                ptx::prefetch_l1(rrow);                   // read chunk by chunk in the epilogue unit
+                ptx::prefetch_l1(static_cast<const char *>(rrow) + 64);
+            }
+        }
+        epi_unit_dispatch<OUT, true>(p.act, tbase + u * COLS, nullptr, rvalid, brow, p.alpha, buf, lane,
+                                     rrow, p.res != nullptr);
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && co_row0 < p.Co) {

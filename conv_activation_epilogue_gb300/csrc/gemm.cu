@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(192, 1)
                 epi_unit_dispatch<OUT, false>(p.act, tbase + u * COLS,
                                               p.bias != nullptr ? p.bias + col0 : nullptr,
                                               p.N - col0, 0.0f, p.alpha, buf, lane,
-                                              residual_row<OUT>(p, row0 + lane, col0));
+                                              residual_row<OUT>(p, row0 + lane, col0), p.res != nullptr);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && row0 < p.M && col0 < p.N) {
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(192, 1)
                 epi_unit_dispatch<OUT, false, 32>(p.act, tbase + (BN / COLS) * COLS,
                                                   p.bias != nullptr ? p.bias + col0 : nullptr,
                                                   p.N - col0, 0.0f, p.alpha, buf, lane,
-                                                  residual_row<OUT>(p, row0 + lane, col0));
+                                                  residual_row<OUT>(p, row0 + lane, col0), p.res != nullptr);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && row0 < p.M && col0 < p.N) {

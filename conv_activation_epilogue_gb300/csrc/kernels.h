@@ -50,6 +50,7 @@ struct ConvArgs {
     const uint16_t *x;
     const uint16_t *w;
     const float *bias;
+    const void *res;     // residual shaped like y (output dtype), or null
     void *y;
     unsigned int *status;
     unsigned long long wait_ns;
@@ -90,6 +91,7 @@ struct NhwcArgs {
     float alpha;
     const void *x;
     const float *bias;   // [Co] or null
+    const void *res;     // residual shaped like y (output dtype), or null
     unsigned int *status;
     unsigned long long wait_ns;
 };

@@ -26,7 +26,7 @@ _lib = None
 # Exported C symbols, as declared in include/mmact.h.
 SYMBOLS = [
     "mmact_gemm", "mmact_gemm_residual", "mmact_gemm_split", "mmact_gemm_split_noalloc", "mmact_conv2d",
-    "mmact_conv2d_split",
+    "mmact_conv2d_split", "mmact_conv2d_residual", "mmact_conv2d_nhwc_residual",
     "mmact_conv2d_nhwc",
     "mmact_conv2d_out_shape", "mmact_conv2d_producer", "mmact_get_last_error",
     "mmact_set_wait_timeout_ns",
@@ -64,6 +64,11 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     L.mmact_conv2d_split.argtypes = conv + [vp, vp]
     L.mmact_conv2d_nhwc.argtypes = conv + [vp]
     L.mmact_conv2d_nhwc.restype = ci
+    conv_res = [vp, vp, vp, vp, vp] + [i64] * 7 + [p_i32, p_i32, p_i32, ci, ci, ci, f32, vp]
+    L.mmact_conv2d_residual.argtypes = conv_res
+    L.mmact_conv2d_residual.restype = ci
+    L.mmact_conv2d_nhwc_residual.argtypes = conv_res
+    L.mmact_conv2d_nhwc_residual.restype = ci
     L.mmact_conv2d_out_shape.argtypes = [i64, i64, i64, i64, p_i32, p_i32, p_i32,
                                          ctypes.POINTER(i64), ctypes.POINTER(i64)]
     L.mmact_conv2d_producer.argtypes = [i64] * 7 + [p_i32, p_i32, p_i32, ci, ci]
@@ -238,6 +243,23 @@ def mmact_conv2d(x, w, bias, y, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1
                           _stream_handle(stream)), "mmact_conv2d")
 
 
+def _residual_ptr(R, y):
+    pr = _dev(R, "R", _OUT)
+    if tuple(R.shape) != tuple(y.shape) or R.dtype != y.dtype:
+        raise ValueError("R must have y's shape and dtype")
+    return pr
+
+
+def mmact_conv2d_residual(x, w, bias, R, y, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1),
+                          act: str = "tanh", alpha: float = 0.0, stream=None) -> None:
+    """y = act(conv2d(x, w) + bias + R), NCHW; R has y's shape and dtype and may be y."""
+    L = load()
+    px, pw, pb, py, *rest = _conv_args(x, w, bias, y, stride, pads, dilation)
+    pr = _residual_ptr(R, y)
+    _check(L.mmact_conv2d_residual(px, pw, pb, pr, py, *rest, DTYPE[x.dtype], DTYPE[y.dtype], ACT[act],
+                                   float(alpha), _stream_handle(stream)), "mmact_conv2d_residual")
+
+
 def mmact_conv2d_split(x, w, bias, y, workspace, stride=(1, 1), pads=(0, 0, 0, 0),
                        dilation=(1, 1), act: str = "tanh", alpha: float = 0.0, stream=None) -> None:
     """Two-kernel ablation of mmact_conv2d through an fp32 workspace shaped like y."""
@@ -255,6 +277,12 @@ def mmact_conv2d_nhwc(x, w, bias, y, stride=(1, 1), pads=(0, 0, 0, 0), dilation=
     """Channels-last y = act(conv2d(x, w) + bias): x [N,H,W,C], w [Co,kh,kw,C], y [N,Ho,Wo,Co].
     x and w may be fp32 (tf32 tensor-core arithmetic, see include/mmact.h)."""
     L = load()
+    px, pw, pb, py, *rest = _nhwc_args(x, w, bias, y, stride, pads, dilation)
+    _check(L.mmact_conv2d_nhwc(px, pw, pb, py, *rest, DTYPE[x.dtype], DTYPE[y.dtype], ACT[act],
+                               float(alpha), _stream_handle(stream)), "mmact_conv2d_nhwc")
+
+
+def _nhwc_args(x, w, bias, y, stride, pads, dilation):
     px = _dev(x, "x", _OUT)
     pw = _dev(w, "w", _OUT)
     py = _dev(y, "y", _OUT)
@@ -267,10 +295,19 @@ def mmact_conv2d_nhwc(x, w, bias, y, stride=(1, 1), pads=(0, 0, 0, 0), dilation=
     Ho, Wo = mmact_conv2d_out_shape(H, W, kh, kw, stride, pads, dilation)
     if tuple(y.shape) != (N, Ho, Wo, Co):
         raise ValueError(f"y must be {(N, Ho, Wo, Co)}")
-    _check(L.mmact_conv2d_nhwc(px, pw, _bias_ptr(bias, Co), py, N, C, H, W, Co, kh, kw,
-                               _i32(stride, 2), _i32(pads, 4), _i32(dilation, 2), DTYPE[x.dtype],
-                               DTYPE[y.dtype], ACT[act], float(alpha), _stream_handle(stream)),
-           "mmact_conv2d_nhwc")
+    return (px, pw, _bias_ptr(bias, Co), py, N, C, H, W, Co, kh, kw, _i32(stride, 2), _i32(pads, 4),
+            _i32(dilation, 2))
+
+
+def mmact_conv2d_nhwc_residual(x, w, bias, R, y, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1),
+                               act: str = "tanh", alpha: float = 0.0, stream=None) -> None:
+    """Channels-last y = act(conv2d(x, w) + bias + R); R has y's shape [N,Ho,Wo,Co] and dtype."""
+    L = load()
+    px, pw, pb, py, *rest = _nhwc_args(x, w, bias, y, stride, pads, dilation)
+    pr = _residual_ptr(R, y)
+    _check(L.mmact_conv2d_nhwc_residual(px, pw, pb, pr, py, *rest, DTYPE[x.dtype], DTYPE[y.dtype],
+                                        ACT[act], float(alpha), _stream_handle(stream)),
+           "mmact_conv2d_nhwc_residual")
 
 
 def mmact_get_last_error(stream=None) -> int:

@@ -4,13 +4,16 @@
  *
  * Operations
  *   C = act(A x B + bias)                        mmact_gemm, mmact_gemm_split
+ *   C = act(A x B + bias + R)                    mmact_gemm_residual
  *     "MatmulLeakyRelu fusion walkthrough" (pyasc examples/05_matmul_leakyrelu):
  *     overview formula C = A x B + Bias then LeakyReLU, computed in one kernel;
  *     sample spec table (A [M,K], B [K,N] row-major and not transposed, bias
  *     fp32 [1,N], C fp32).  ReLU: "ops-nn fused_matmul_relu" article, the
  *     fused call on 4096^3 and its two-call fallback (matmul into a device
  *     temporary, then relu).
- *   y = act(conv2d(x, w, bias))                  mmact_conv2d, mmact_conv2d_split
+ *   y = act(conv2d(x, w, bias))                  mmact_conv2d, mmact_conv2d_split,
+ *                                                mmact_conv2d_nhwc (channels-last)
+ *   y = act(conv2d(x, w, bias) + R)              mmact_conv2d_residual, mmact_conv2d_nhwc_residual
  *     "multimodal-ops Fused ConvTanh" article: y = tanh(conv2d(x, filter,
  *     bias)) with strides / pads / dilations; the convolution is an implicit
  *     GEMM whose A operand is the filter [Co x Ci*kh*kw] and whose B operand is
@@ -148,6 +151,24 @@ mmact_status mmact_conv2d(const void *x, const void *w, const float *bias, void 
                           mmact_act act, float alpha, void *stream);
 
 /*
+ * mmact_conv2d with a residual tensor added before the activation:
+ *   y = act(conv2d(x, w) + bias + R), the conv form of mmact_gemm_residual
+ *   (the fused_matmul_relu article's element-wise add fused into the
+ *   preceding computation, as in residual networks).
+ *   R  [N, Co, Ho, Wo] in out_dtype (y's shape), 16-byte aligned; read, never
+ *      written.  R == y is allowed; any other overlap of R and y returns
+ *      MMACT_ERR_INVALID_ARG.  R may be NULL only if y is empty.
+ * Everything else as mmact_conv2d (C == 0 gives y = act(bias + R)).
+ */
+mmact_status mmact_conv2d_residual(const void *x, const void *w, const float *bias, const void *R,
+                                   void *y, int64_t N, int64_t C, int64_t H, int64_t W,
+                                   int64_t Co, int64_t kh, int64_t kw,
+                                   const int32_t strides[2], const int32_t pads[4],
+                                   const int32_t dilations[2],
+                                   mmact_dtype in_dtype, mmact_dtype out_dtype,
+                                   mmact_act act, float alpha, void *stream);
+
+/*
  * Two-kernel ablation of mmact_conv2d: kernel 1 writes z (conv + bias, fp32)
  * to `workspace` ([N, Co, Ho, Wo] fp32, caller-allocated, 16-byte aligned),
  * kernel 2 applies act and writes y.
@@ -219,6 +240,20 @@ mmact_status mmact_conv2d_nhwc(const void *x, const void *w, const float *bias, 
                                const int32_t dilations[2],
                                mmact_dtype in_dtype, mmact_dtype out_dtype,
                                mmact_act act, float alpha, void *stream);
+
+/*
+ * mmact_conv2d_nhwc with a residual tensor added before the activation:
+ *   y = act(conv2d(x, w) + bias + R), R [N, Ho, Wo, Co] in out_dtype (y's
+ *   shape), 16-byte aligned; R == y allowed, other overlaps rejected with
+ *   MMACT_ERR_INVALID_ARG.  Everything else as mmact_conv2d_nhwc.
+ */
+mmact_status mmact_conv2d_nhwc_residual(const void *x, const void *w, const float *bias, const void *R,
+                                        void *y, int64_t N, int64_t C, int64_t H, int64_t W,
+                                        int64_t Co, int64_t kh, int64_t kw,
+                                        const int32_t strides[2], const int32_t pads[4],
+                                        const int32_t dilations[2],
+                                        mmact_dtype in_dtype, mmact_dtype out_dtype,
+                                        mmact_act act, float alpha, void *stream);
 
 /*
  * Output spatial size of a conv geometry (host only, no CUDA call).  Writes
