@@ -186,9 +186,12 @@ def workload_bytes(mmact, wl):
 class NhwcProblem:
     """A conv workload in channels-last layout (same values, transposed on the host)."""
 
+    layout = "nhwc"
+
     def __init__(self, torch, mmact, wl, device, inputs=None, fp32_inputs=False):
         self.mmact, self.wl = mmact, wl
         inp = inputs if inputs is not None else wl.inputs()
+        self.host = inp
         x = np.ascontiguousarray(inp["x"].transpose(0, 2, 3, 1))
         w = np.ascontiguousarray(inp["w"].transpose(0, 2, 3, 1))
         if fp32_inputs:
@@ -201,6 +204,9 @@ class NhwcProblem:
         self.bias = torch.from_numpy(inp["bias"]).to(device)
         Ho, Wo = mmact.mmact_conv2d_out_shape(wl.H, wl.W, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation)
         self.out = torch.empty((wl.N, Ho, Wo, wl.Co), dtype=torch_dtype(torch, wl.out_dtype), device=device)
+
+    def input_bytes(self):
+        return sum(t.numel() * t.element_size() for t in (self.x, self.w, self.bias))
 
     def run(self, variant="fused", stream=None):
         wl = self.wl
@@ -304,7 +310,10 @@ def time_graph(torch, fn, reps, stream):
 def parity_spot_check(oracle_mod, prob, npts=256, seed=99):
     """Compare a few sampled outputs of the timed launch with the oracle (max err / bound)."""
     wl = prob.wl
-    out = prob.out.float().cpu().numpy().astype(np.float64).ravel()
+    out = prob.out
+    if getattr(prob, "layout", "nchw") == "nhwc":
+        out = out.permute(0, 3, 1, 2)            # compare in the oracle's NCHW order
+    out = out.float().cpu().numpy().astype(np.float64).ravel()
     rng = np.random.default_rng(seed)
     pts = rng.integers(0, out.size, size=npts)
     orc = oracle_mod.get()
@@ -416,6 +425,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sustained", action="store_true")
+    ap.add_argument("--layout", default="nchw", choices=["nchw", "nhwc"],
+                    help="conv workloads: time the channels-last kernel (same values, transposed)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -440,7 +451,10 @@ def main():
             dist.barrier()
 
     wl = synth.WORKLOADS[args.workload]
-    prob = Problem(torch, mmact, wl, device)
+    if args.layout == "nhwc" and wl.kind == "conv":
+        prob = NhwcProblem(torch, mmact, wl, device)
+    else:
+        prob = Problem(torch, mmact, wl, device)
     flops = workload_flops(mmact, wl)
     stream = torch.cuda.current_stream()
 
@@ -497,7 +511,15 @@ def main():
     if sustained is not None:
         sustained["frac_of_sustained_peak"] = sustained["tflops"] / peaks["bf16_tflops_sustained"]
     achieved = flops / (ms * 1e-3) / 1e12        # one launch per step
-    kname = "gemm_act_kernel" if wl.kind == "gemm" else "conv_act_kernel"
+    if wl.kind == "gemm":
+        kname = "gemm_act_kernel"
+    elif getattr(prob, "layout", "nchw") == "nhwc":
+        kname = "conv_nhwc_kernel"
+    else:
+        producer = mmact.mmact_conv2d_producer(wl.N, wl.C, wl.H, wl.W, wl.Co, wl.kh, wl.kw, wl.stride,
+                                               wl.pads, wl.dilation, torch_dtype(torch, wl.dtype),
+                                               torch_dtype(torch, wl.out_dtype))
+        kname = "conv_act_kernel" if producer == "gather" else "conv_vec_kernel"
     in_bytes = prob.input_bytes()
 
     # --- end to end through the public API with host buffers
@@ -511,6 +533,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.ab_dtype if wl.kind == "gemm" else wl.dtype, "data": "synthetic",
         "config": {"workload": wl.name, "variant": "fused single kernel",
+                   "layout": getattr(prob, "layout", "nchw") if wl.kind == "conv" else "row-major",
                    "l2": "inputs larger than L2, no flush" if in_bytes > L2_BYTES
                    else "inputs smaller than L2, no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU",
@@ -545,8 +568,12 @@ def end_to_end(torch, mmact, wl, prob, device, stream, args, flops, world, barri
         hb = torch.from_numpy(h["bias"]).pin_memory()
         hosts, devs = (hA, hB, hb), (prob.A, prob.B, prob.bias)
     else:
-        hx = codes_to(torch, h["x"], wl.dtype, "cpu", pin=True)
-        hw = codes_to(torch, h["w"], wl.dtype, "cpu", pin=True)
+        x, w = h["x"], h["w"]
+        if getattr(prob, "layout", "nchw") == "nhwc":
+            x = np.ascontiguousarray(x.transpose(0, 2, 3, 1))
+            w = np.ascontiguousarray(w.transpose(0, 2, 3, 1))
+        hx = codes_to(torch, x, wl.dtype, "cpu", pin=True)
+        hw = codes_to(torch, w, wl.dtype, "cpu", pin=True)
         hb = torch.from_numpy(h["bias"]).pin_memory()
         hosts, devs = (hx, hw, hb), (prob.x, prob.w, prob.bias)
     hout = torch.empty(prob.out.shape, dtype=prob.out.dtype).pin_memory()
