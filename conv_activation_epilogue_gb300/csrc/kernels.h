@@ -26,6 +26,7 @@ struct GemmLaunch {
     int tile_n;          // 64, 128, 192, 224 or 256
     int out;             // OUT_*
     int grid;
+    int split_k;         // 0: persistent kernel; 2 or 4: split-K cluster kernel (tile_n 256)
 };
 
 struct ConvArgs {
@@ -107,6 +108,12 @@ struct NhwcLaunch {
 cudaError_t setup_nhwc_kernels();
 cudaError_t launch_conv_nhwc(const NhwcLaunch &L, cudaStream_t stream);
 cudaError_t launch_gemm(const GemmLaunch &L, cudaStream_t stream);
+// Split-K over a cluster of L.split_k CTAs, one 128 x 256 tile per cluster
+// (grid = tiles x split_k); no residual.
+cudaError_t setup_splitk_kernels();
+cudaError_t launch_gemm_splitk(const GemmLaunch &L, cudaStream_t stream);
+// Split-K clusters of S CTAs that fit on the device at once (0: unknown).
+int splitk_max_clusters(int S);
 cudaError_t launch_conv(const ConvLaunch &L, cudaStream_t stream);
 // out[i] = act(ws[i]) for i < count (ws fp32, out of dtype `out`).
 cudaError_t launch_act(const float *ws, void *out, int64_t count, int out_kind, int act,

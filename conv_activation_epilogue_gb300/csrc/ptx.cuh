@@ -35,6 +35,45 @@ __device__ __forceinline__ void prefetch_l1(const void *p)
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
+// ------------------------------------------------------------------ clusters --
+// Rank of this CTA in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Cluster-wide barrier, one phase: every thread of every CTA of the cluster
+// arrives (release) and waits (acquire).  Shared-memory writes made before
+// it are visible to the cluster's CTAs after it.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Address, in CTA `rank` of the cluster, of the shared-memory location that
+// `addr` names in this CTA.
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory to another CTA's (dst from mapa); completion
+// is signalled as transaction bytes on the destination CTA's mbarrier
+// (bar from mapa).  The source must have been written through the async
+// proxy or made visible to it (fence_proxy_async_smem).
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                     uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // ----------------------------------------------- programmatic dependent launch --
 // Lets the next kernel in the stream be scheduled now (its blocks still wait
 // in griddep_wait until this grid has finished).  No effect when the launch

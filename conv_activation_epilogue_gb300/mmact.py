@@ -30,7 +30,8 @@ SYMBOLS = [
     "mmact_conv2d_nhwc",
     "mmact_conv2d_out_shape", "mmact_conv2d_producer", "mmact_get_last_error",
     "mmact_set_wait_timeout_ns",
-    "mmact_selftest_wait_timeout", "mmact_set_gemm_tile_n", "mmact_status_string", "mmact_version",
+    "mmact_selftest_wait_timeout", "mmact_set_gemm_tile_n", "mmact_set_gemm_split_k",
+    "mmact_gemm_split_k_choice", "mmact_status_string", "mmact_version",
 ]
 
 
@@ -78,12 +79,15 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     L.mmact_set_wait_timeout_ns.restype = None
     L.mmact_selftest_wait_timeout.argtypes = [u64, vp]
     L.mmact_set_gemm_tile_n.argtypes = [ci]
+    L.mmact_set_gemm_split_k.argtypes = [ci]
+    L.mmact_gemm_split_k_choice.argtypes = [i64, i64, i64, ci, ctypes.POINTER(ci)]
     L.mmact_status_string.argtypes = [ci]
     L.mmact_status_string.restype = ctypes.c_char_p
     L.mmact_version.argtypes = []
     for name in ("mmact_gemm", "mmact_gemm_split", "mmact_conv2d", "mmact_conv2d_split",
                  "mmact_conv2d_out_shape", "mmact_get_last_error", "mmact_selftest_wait_timeout",
-                 "mmact_set_gemm_tile_n", "mmact_version"):
+                 "mmact_set_gemm_tile_n", "mmact_set_gemm_split_k", "mmact_gemm_split_k_choice",
+                 "mmact_version"):
         getattr(L, name).restype = ci
     _lib = L
     return L
@@ -326,6 +330,19 @@ def mmact_selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
 
 def mmact_set_gemm_tile_n(tile_n: int) -> None:
     _check(load().mmact_set_gemm_tile_n(int(tile_n)), "mmact_set_gemm_tile_n")
+
+
+def mmact_set_gemm_split_k(split_k: int) -> None:
+    """0: split-K chosen per shape; 1: never; 2 or 4: whenever legal."""
+    _check(load().mmact_set_gemm_split_k(int(split_k)), "mmact_set_gemm_split_k")
+
+
+def mmact_gemm_split_k_choice(M: int, N: int, K: int, residual: bool = False) -> int:
+    """Split-K factor (0, 2 or 4) a GEMM of this shape would use on the current device."""
+    out = ctypes.c_int(-1)
+    _check(load().mmact_gemm_split_k_choice(int(M), int(N), int(K), 1 if residual else 0,
+                                            ctypes.byref(out)), "mmact_gemm_split_k_choice")
+    return out.value
 
 
 def mmact_status_string(status: int) -> str:
