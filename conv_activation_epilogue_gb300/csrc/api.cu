@@ -152,17 +152,16 @@ int choose_tile_n(int64_t tiles_m, int64_t N, int sms)
 // the cluster barriers).  It is taken when all its clusters are resident at
 // once (one wave) and each CTA still has enough K blocks to amortise that
 // cost: at least 16 with S = 4, at least 64 with S = 2 (S = 2 halves the
-// per-CTA work only twice for the same exchange cost), and never with a
-// residual.  Measured on GB300 against the persistent kernel's own choice of
+// per-CTA work only twice for the same exchange cost).  Measured on GB300 against the persistent kernel's own choice of
 // tile (bf16, us): 128x8192x8192 39.4 -> 30.7 (S=4); 1024x1024x8192 38.8 ->
 // 21.3 (4); 256x4096x8192 38.8 -> 22.2 (4); 128x4096x4096 21.0 -> 15.2 (4);
 // 384x2048x4096 21.1 -> 16.0 (4); 256x8192x8192 40.7 -> 36.2 (2); and
 // 128x16384x4096 27.4 vs 29.3 with S=2, where the rule keeps the persistent
 // kernel (32 K blocks per CTA).
-int choose_split_k(const DeviceInfo &dev, int64_t tiles_m, int64_t N, int64_t num_kb, bool has_res)
+int choose_split_k(const DeviceInfo &dev, int64_t tiles_m, int64_t N, int64_t num_kb)
 {
     const int mode = g_split_k.load();
-    if (has_res || mode == 1) return 0;
+    if (mode == 1) return 0;
     const int64_t tiles = tiles_m * ((N + 255) / 256);
     if (mode == 2 || mode == 4) return num_kb >= mode ? mode : 0;
     if (g_tile_n.load() != 0) return 0;   // a fixed tile width asks for the persistent kernel
@@ -187,7 +186,7 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
     GemmLaunch L;
     std::memset(&L, 0, sizeof(L));
     const int tiles_m = (int)((M + 127) / 128);
-    const int split = choose_split_k(*dev, tiles_m, N, (K + 63) / 64, res != nullptr);
+    const int split = choose_split_k(*dev, tiles_m, N, (K + 63) / 64);
     int bn = split != 0 ? 256 : g_tile_n.load();
     if (bn == 0) bn = choose_tile_n(tiles_m, N, dev->sm_count);
     const int tiles_n = (int)((N + bn - 1) / bn);
@@ -760,8 +759,7 @@ MMACT_EXPORT mmact_status mmact_set_gemm_tile_n(int tile_n)
     return MMACT_OK;
 }
 
-MMACT_EXPORT mmact_status mmact_gemm_split_k_choice(int64_t M, int64_t N, int64_t K, int has_residual,
-                                                    int *split_k)
+MMACT_EXPORT mmact_status mmact_gemm_split_k_choice(int64_t M, int64_t N, int64_t K, int *split_k)
 {
     if (split_k == nullptr || M < 0 || N < 0 || K < 0) return MMACT_ERR_INVALID_ARG;
     DeviceInfo *dev = nullptr;
@@ -769,7 +767,7 @@ MMACT_EXPORT mmact_status mmact_gemm_split_k_choice(int64_t M, int64_t N, int64_
     if (st != MMACT_OK) return st;
     *split_k = (M == 0 || N == 0 || K == 0)
                    ? 0
-                   : choose_split_k(*dev, (M + 127) / 128, N, (K + 63) / 64, has_residual != 0);
+                   : choose_split_k(*dev, (M + 127) / 128, N, (K + 63) / 64);
     return MMACT_OK;
 }
 

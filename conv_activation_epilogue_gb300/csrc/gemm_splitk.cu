@@ -23,8 +23,8 @@
 //               completes on the owner's receive mbarrier;
 //               (b) wait for the S-1 incoming slices, add them to this CTA's
 //                   own slice (256/S columns) of its TMEM accumulator, then
-//                   bias, activation, conversion and TMA store as in the
-//                   persistent kernel;
+//                   the residual (if any), bias, activation, conversion and
+//                   TMA store as in the persistent kernel;
 //               cluster barrier (no CTA leaves while a copy is in flight).
 //
 // The exchange moves 32 KB blocks through the copy engine: reading the
@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(192, 1)
     constexpr int STAGES = Cfg::STAGES;
     constexpr int SLICE = Cfg::SLICE;
     constexpr int COLS = OUT == OUT_F32 ? 32 : 64;   // output columns per 128-byte staging row
+    constexpr int ESZ = OUT == OUT_F32 ? 4 : 2;      // output (and residual) element bytes
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t base = ptx::smem_addr(smem);
@@ -325,10 +326,18 @@ __global__ void __launch_bounds__(192, 1)
 
     if (aligned && warp >= 2) {
         // -------------------------- epilogue (b): finish this CTA's slice --
-        // the slice's bias lines, fetched while the peers' slices arrive
+        // the slice's bias lines and this lane's residual row segment,
+        // fetched while the peers' slices arrive
         const int slice0 = nb * Cfg::BN + (int)rank * SLICE;
         if (p.bias != nullptr && warp == 2 && lane < SLICE / 32 && slice0 + 32 * lane < p.N)
             ptx::prefetch_l1(p.bias + slice0 + 32 * lane);
+        const char *res_row = nullptr;                   // residual at (row m, column slice0)
+        if (p.res != nullptr && mb * 128 + m < p.M) {
+            res_row = static_cast<const char *>(p.res) + ((int64_t)(mb * 128 + m) * p.N + slice0) * ESZ;
+#pragma unroll
+            for (int b = 0; b < SLICE * ESZ; b += 128)
+                if (slice0 + b / ESZ < p.N) ptx::prefetch_l1(res_row + b);
+        }
         // The peers' slices of this CTA's columns.  Every aligned CTA sends,
         // failed or not, and this wait does not give up on an abort: no copy
         // may still be writing into this CTA's shared memory when it exits.
@@ -376,6 +385,9 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
                 const int c32 = col0 + 32 * h;
+                if (p.res != nullptr)                    // warp-uniform; null rows add nothing
+                    add_residual<OUT, 32>(res_row != nullptr ? res_row + (scol + 32 * h) * ESZ : nullptr,
+                                          p.N - c32, v);
                 finish32_act<OUT>(p.act, v, p.bias != nullptr ? p.bias + c32 : nullptr, p.N - c32,
                                   p.alpha, row, sw, 4 * h);
             }

@@ -109,7 +109,7 @@ cudaError_t setup_nhwc_kernels();
 cudaError_t launch_conv_nhwc(const NhwcLaunch &L, cudaStream_t stream);
 cudaError_t launch_gemm(const GemmLaunch &L, cudaStream_t stream);
 // Split-K over a cluster of L.split_k CTAs, one 128 x 256 tile per cluster
-// (grid = tiles x split_k); no residual.
+// (grid = tiles x split_k).
 cudaError_t setup_splitk_kernels();
 cudaError_t launch_gemm_splitk(const GemmLaunch &L, cudaStream_t stream);
 // Split-K clusters of S CTAs that fit on the device at once (0: unknown).

@@ -80,7 +80,7 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     L.mmact_selftest_wait_timeout.argtypes = [u64, vp]
     L.mmact_set_gemm_tile_n.argtypes = [ci]
     L.mmact_set_gemm_split_k.argtypes = [ci]
-    L.mmact_gemm_split_k_choice.argtypes = [i64, i64, i64, ci, ctypes.POINTER(ci)]
+    L.mmact_gemm_split_k_choice.argtypes = [i64, i64, i64, ctypes.POINTER(ci)]
     L.mmact_status_string.argtypes = [ci]
     L.mmact_status_string.restype = ctypes.c_char_p
     L.mmact_version.argtypes = []
@@ -337,11 +337,11 @@ def mmact_set_gemm_split_k(split_k: int) -> None:
     _check(load().mmact_set_gemm_split_k(int(split_k)), "mmact_set_gemm_split_k")
 
 
-def mmact_gemm_split_k_choice(M: int, N: int, K: int, residual: bool = False) -> int:
+def mmact_gemm_split_k_choice(M: int, N: int, K: int) -> int:
     """Split-K factor (0, 2 or 4) a GEMM of this shape would use on the current device."""
     out = ctypes.c_int(-1)
-    _check(load().mmact_gemm_split_k_choice(int(M), int(N), int(K), 1 if residual else 0,
-                                            ctypes.byref(out)), "mmact_gemm_split_k_choice")
+    _check(load().mmact_gemm_split_k_choice(int(M), int(N), int(K), ctypes.byref(out)),
+           "mmact_gemm_split_k_choice")
     return out.value
 
 

@@ -316,13 +316,13 @@ mmact_status mmact_set_gemm_tile_n(int tile_n);
 
 /*
  * Tuning and testing aid: the split-K GEMM kernel.  For GEMMs with few
- * 128 x 256 output tiles (small M) mmact_gemm, mmact_gemm_split and
- * mmact_gemm_split_noalloc may run each tile on a thread-block cluster of 2
- * or 4 CTAs, each CTA accumulating 1/2 or 1/4 of the K blocks, the partial
- * fp32 tiles summed across the cluster before the same bias + activation
- * epilogue (the sum over K stays in fp32).  split_k: 0 = chosen per shape
- * (the default), 1 = never, 2 or 4 = always with that factor when the call
- * has no residual and K has at least that many 64-wide blocks.  Applies to
+ * 128 x 256 output tiles (small M) mmact_gemm, mmact_gemm_residual,
+ * mmact_gemm_split and mmact_gemm_split_noalloc may run each tile on a
+ * thread-block cluster of 2 or 4 CTAs, each CTA accumulating 1/2 or 1/4 of
+ * the K blocks, the partial fp32 tiles summed across the cluster before the
+ * same residual + bias + activation epilogue (the sum over K stays in fp32).
+ * split_k: 0 = chosen per shape (the default), 1 = never, 2 or 4 = always
+ * with that factor when K has at least that many 64-wide blocks.  Applies to
  * later calls in the process.  Returns MMACT_ERR_INVALID_ARG for other values.
  */
 mmact_status mmact_set_gemm_split_k(int split_k);
@@ -330,13 +330,11 @@ mmact_status mmact_set_gemm_split_k(int split_k);
 /*
  * The split-K factor (0 = none, 2 or 4) that an mmact_gemm-family call of
  * this shape on the current device would use under the current setting of
- * mmact_set_gemm_split_k and mmact_set_gemm_tile_n; has_residual != 0 for
- * mmact_gemm_residual.  Writes it to *split_k.  Returns MMACT_ERR_INVALID_ARG
- * for a null split_k or a negative extent, MMACT_ERR_CUDA when the device
- * cannot be queried.
+ * mmact_set_gemm_split_k and mmact_set_gemm_tile_n.  Writes it to *split_k.
+ * Returns MMACT_ERR_INVALID_ARG for a null split_k or a negative extent,
+ * MMACT_ERR_CUDA when the device cannot be queried.
  */
-mmact_status mmact_gemm_split_k_choice(int64_t M, int64_t N, int64_t K, int has_residual,
-                                       int *split_k);
+mmact_status mmact_gemm_split_k_choice(int64_t M, int64_t N, int64_t K, int *split_k);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *mmact_status_string(mmact_status status);

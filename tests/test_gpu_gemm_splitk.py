@@ -5,8 +5,9 @@ of 2 or 4 CTAs, each over its share of the K blocks, and the fp32 partial
 tiles are summed across the cluster before the bias + activation epilogue.
 The mode switch forces the kernel onto small shapes that span several tiles,
 ragged M / N / K tails, K-block counts not divisible by the split factor
-(down to one block per CTA), every output dtype and every activation; the
-skinny full-size workload is checked through the automatic choice.
+(down to one block per CTA), every output dtype and every activation, with
+and without a residual (also in place); the skinny full-size workload is
+checked through the automatic choice.
 """
 import numpy as np
 import pytest
@@ -123,22 +124,46 @@ def test_cancellation_across_cluster_partials(orc):
     check(host(C), ref, "f32", "cancellation")
 
 
-def test_residual_calls_keep_the_persistent_kernel(orc):
-    mmact.mmact_set_gemm_split_k(4)
+@pytest.mark.parametrize("S", [2, 4])
+@pytest.mark.parametrize("cd", ["bf16", "f32"])
+def test_forced_split_k_residual(orc, S, cd):
+    # C = act(A @ B + bias + R), R in the output dtype; ragged M and N
+    rng = np.random.default_rng(50 + S + len(cd))
+    M, N, K = 200, 392, 1024
+    A = rand_codes(rng, (M, K), "bf16")
+    B = rand_codes(rng, (K, N), "bf16")
+    bias = rng.uniform(-1, 1, N).astype(np.float32)
+    R = rand_codes(rng, (M, N), cd) if cd != "f32" else rng.uniform(-1, 1, (M, N)).astype(np.float32)
+    mmact.mmact_set_gemm_split_k(S)
     try:
-        assert mmact.mmact_gemm_split_k_choice(128, 512, 1024, residual=True) == 0
-        rng = np.random.default_rng(5)
-        M, N, K = 128, 512, 1024
-        A = rand_codes(rng, (M, K), "bf16")
-        B = rand_codes(rng, (K, N), "bf16")
-        bias = rng.uniform(-1, 1, N).astype(np.float32)
-        R = rand_codes(rng, (M, N), "bf16")
-        C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        assert mmact.mmact_gemm_split_k_choice(M, N, K) == S
+        C = torch.full((M, N), float("nan"), dtype=TORCH[cd], device="cuda")
         mmact.mmact_gemm_residual(to_device(A, "bf16"), to_device(B, "bf16"), fp32_to_device(bias),
-                                  to_device(R, "bf16"), C, "relu", 0.0)
+                                  fp32_to_device(R) if cd == "f32" else to_device(R, cd), C, "relu", 0.0)
         assert mmact.mmact_get_last_error() == mmact.MMACT_OK
-        check(host(C), orc.gemm(A, B, "bf16", bias, "relu", 0.0, residual=R, res_dtype="bf16"), "bf16",
-              "residual")
+        check(host(C), orc.gemm(A, B, "bf16", bias, "relu", 0.0, residual=R, res_dtype=cd), cd,
+              f"S={S} residual {cd}")
+    finally:
+        mmact.mmact_set_gemm_split_k(0)
+
+
+@pytest.mark.parametrize("S", [2, 4])
+def test_forced_split_k_residual_in_place(orc, S):
+    # R is C itself: every element is read before its own unit's store writes it
+    rng = np.random.default_rng(60 + S)
+    M, N, K = 256, 512, 512
+    A = rand_codes(rng, (M, K), "bf16")
+    B = rand_codes(rng, (K, N), "bf16")
+    bias = rng.uniform(-1, 1, N).astype(np.float32)
+    R = rand_codes(rng, (M, N), "bf16")
+    mmact.mmact_set_gemm_split_k(S)
+    try:
+        C = to_device(R, "bf16").clone()
+        mmact.mmact_gemm_residual(to_device(A, "bf16"), to_device(B, "bf16"), fp32_to_device(bias), C, C,
+                                  "gelu", 0.0)
+        assert mmact.mmact_get_last_error() == mmact.MMACT_OK
+        check(host(C), orc.gemm(A, B, "bf16", bias, "gelu", residual=R, res_dtype="bf16"), "bf16",
+              f"S={S} in place")
     finally:
         mmact.mmact_set_gemm_split_k(0)
 
