@@ -35,7 +35,7 @@ from conv_activation_epilogue_gb300 import synth  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "fused GEMM/conv+act TFLOP/s and % of GB300 dense bf16 tensor peak (1 GPU)"
-KERNEL_SOURCES = ["common.cuh", "ptx.cuh", "gemm.cu", "gemm_splitk.cu", "conv.cu", "conv_vec.cu", "conv_nhwc.cu", "elementwise.cu", "api.cu"]
+KERNEL_SOURCES = ["common.cuh", "ptx.cuh", "gemm.cu", "gemm_splitk.cu", "gemm_pair.cu", "conv.cu", "conv_vec.cu", "conv_nhwc.cu", "elementwise.cu", "api.cu"]
 
 
 def env_int(name, default):
@@ -512,7 +512,8 @@ def main():
         sustained["frac_of_sustained_peak"] = sustained["tflops"] / peaks["bf16_tflops_sustained"]
     achieved = flops / (ms * 1e-3) / 1e12        # one launch per step
     if wl.kind == "gemm":
-        kname = "gemm_splitk_kernel" if mmact.mmact_gemm_split_k_choice(wl.M, wl.N, wl.K) else "gemm_act_kernel"
+        kname = {"pair": "gemm_pair_kernel", "split_k": "gemm_splitk_kernel"}.get(
+            mmact.mmact_gemm_kernel_choice(wl.M, wl.N, wl.K), "gemm_act_kernel")
     elif getattr(prob, "layout", "nchw") == "nhwc":
         kname = "conv_nhwc_kernel"
     else:
@@ -667,17 +668,22 @@ def sweep(torch, mmact, device, stream, peaks):
         # the fused-vs-split decision, re-measured on every run
         rec["fused_speedup_over_split"] = round(rec["split"]["ms"] / rec["fused"]["ms"], 3)
         if wl.kind == "gemm":
-            # the split-K choice (cluster of S CTAs per tile), and the persistent kernel beside it
+            # the GEMM kernel the planner chose (persistent, CTA pair or split-K cluster), and
+            # the one-SM persistent kernel beside it when it is not that one
+            rec["kernel"] = mmact.mmact_gemm_kernel_choice(wl.M, wl.N, wl.K)
             rec["split_k"] = mmact.mmact_gemm_split_k_choice(wl.M, wl.N, wl.K)
-            if rec["split_k"]:
+            if rec["kernel"] != "persistent":
                 mmact.mmact_set_gemm_split_k(1)
+                mmact.mmact_set_gemm_pair(1)
                 try:
                     ms = time_graph(torch, lambda: prob.run("fused"), 20, stream)
                 finally:
                     mmact.mmact_set_gemm_split_k(0)
+                    mmact.mmact_set_gemm_pair(0)
                 tf = flops / (ms * 1e-3) / 1e12
-                rec["fused_without_split_k"] = {"ms": round(ms, 5), "tflops": round(tf, 2),
-                                                "alg_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+                rec["fused_persistent_kernel"] = {"ms": round(ms, 5), "tflops": round(tf, 2),
+                                                  "pct_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 2),
+                                                  "alg_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
         if wl.kind == "conv":
             rec["nchw_producer"] = mmact.mmact_conv2d_producer(
                 wl.N, wl.C, wl.H, wl.W, wl.Co, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation,

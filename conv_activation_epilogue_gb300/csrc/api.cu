@@ -29,12 +29,14 @@ constexpr uint64_t DEFAULT_WAIT_NS = 2000000000ull;
 std::atomic<uint64_t> g_wait_ns{DEFAULT_WAIT_NS};
 std::atomic<int> g_tile_n{0};
 std::atomic<int> g_split_k{0};   // 0: chosen per shape; 1: never; 2 or 4: whenever legal
+std::atomic<int> g_pair{0};      // CTA-pair GEMM kernel: 0 chosen per shape; 1 never; 2 always
 
 constexpr int MAX_DEVICES = 64;
 struct DeviceInfo {
     bool ready = false;
     int sm_count = 0;
     int splitk_clusters[2] = {0, 0};  // resident split-K clusters of 2 and of 4 CTAs
+    int pair_clusters = 0;            // resident CTA pairs of the pair kernel
     unsigned int *status = nullptr;   // device address of g_status
 };
 DeviceInfo g_dev[MAX_DEVICES];
@@ -59,8 +61,9 @@ mmact_status device_info(DeviceInfo **out)
             return MMACT_ERR_CUDA;
         if (setup_gemm_kernels() != cudaSuccess || setup_conv_kernels() != cudaSuccess ||
             setup_conv_vec_kernels() != cudaSuccess || setup_nhwc_kernels() != cudaSuccess ||
-            setup_splitk_kernels() != cudaSuccess)
+            setup_splitk_kernels() != cudaSuccess || setup_pair_kernels() != cudaSuccess)
             return MMACT_ERR_CUDA;
+        d.pair_clusters = pair_max_clusters();
         d.splitk_clusters[0] = splitk_max_clusters(2);
         d.splitk_clusters[1] = splitk_max_clusters(4);
         if (g_encode == nullptr) {
@@ -170,6 +173,33 @@ int choose_split_k(const DeviceInfo &dev, int64_t tiles_m, int64_t N, int64_t nu
     return 0;
 }
 
+// Whether a GEMM that takes neither split-K nor a forced tile width runs on
+// the CTA-pair kernel: 256 x 256 tiles on pairs of SMs, one M = 256
+// tcgen05.mma per pair (each SM fills 32 KB of shared memory per K block
+// instead of 48 KB for the same MMA work).  Taken when the persistent kernel
+// would use 256-wide tiles and the pair grid needs no more waves than the
+// persistent one: each wave of either does 128 x 256 outputs per SM, and a
+// pair wave was measured faster (bf16 on GB300: 8192^3 639 -> 577 us,
+// 8192x8192x4096 326 -> 282, 4096^3 94.6 -> 81.8, 16384x4096x1024
+// 89.8 -> 82.8).  Not with a residual over 16 or fewer K blocks: there the
+// epilogue (which reads the residual) outlasts the main loop, and a pair
+// releases its accumulator only when both CTAs' epilogues are done
+// (16384x4096x1024 with residual: 103 us persistent, 116 us pair).
+bool choose_pair(const DeviceInfo &dev, int64_t M, int64_t N, int64_t num_kb, bool has_res)
+{
+    const int mode = g_pair.load();
+    if (mode == 1 || dev.pair_clusters <= 0) return false;
+    if (mode == 2) return true;
+    if (g_tile_n.load() != 0) return false;
+    if (has_res && num_kb <= 16) return false;
+    const int64_t tiles_m = (M + 127) / 128;
+    if (choose_tile_n(tiles_m, N, dev.sm_count) != 256) return false;
+    const int64_t tiles_n = (N + 255) / 256;
+    const int64_t waves = (tiles_m * tiles_n + dev.sm_count - 1) / dev.sm_count;
+    const int64_t pair_waves = (((M + 255) / 256) * tiles_n + dev.pair_clusters - 1) / dev.pair_clusters;
+    return pair_waves <= waves;
+}
+
 // Shared by mmact_gemm, mmact_gemm_residual and the first kernel of
 // mmact_gemm_split.  `res`: residual [M, N] in the output dtype, or null.
 mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void *C, int64_t M,
@@ -187,7 +217,8 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
     std::memset(&L, 0, sizeof(L));
     const int tiles_m = (int)((M + 127) / 128);
     const int split = choose_split_k(*dev, tiles_m, N, (K + 63) / 64);
-    int bn = split != 0 ? 256 : g_tile_n.load();
+    const bool pair = split == 0 && choose_pair(*dev, M, N, (K + 63) / 64, res != nullptr);
+    int bn = split != 0 || pair ? 256 : g_tile_n.load();
     if (bn == 0) bn = choose_tile_n(tiles_m, N, dev->sm_count);
     const int tiles_n = (int)((N + bn - 1) / bn);
     GemmArgs &a = L.args;
@@ -210,6 +241,13 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
     L.out = out_kind(cd);
     L.grid = (int)std::min<int64_t>(a.num_tiles, dev->sm_count);
     L.split_k = split;
+    if (pair) {
+        // 256 x 256 tiles, one per CTA pair
+        a.tiles_m = (int)((M + 255) / 256);
+        a.num_tiles = a.tiles_m * tiles_n;
+        L.pair = 1;
+        L.grid = 2 * (int)std::min<int64_t>(a.num_tiles, dev->pair_clusters);
+    }
     if (split != 0) {
         if ((int64_t)a.num_tiles * split > MAX_DIM) return MMACT_ERR_UNSUPPORTED;
         L.grid = a.num_tiles * split;   // one cluster per tile
@@ -229,7 +267,9 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
         const uint32_t bT[2] = {32, 32};
         if (!encode(&L.tmCt, cd, 2, C, dC, sC, bT, false)) return MMACT_ERR_CUDA;
     }
-    const cudaError_t e = split != 0 ? launch_gemm_splitk(L, stream) : launch_gemm(L, stream);
+    const cudaError_t e = split != 0 ? launch_gemm_splitk(L, stream)
+                          : pair       ? launch_gemm_pair(L, stream)
+                                       : launch_gemm(L, stream);
     return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
 }
 
@@ -768,6 +808,31 @@ MMACT_EXPORT mmact_status mmact_gemm_split_k_choice(int64_t M, int64_t N, int64_
     *split_k = (M == 0 || N == 0 || K == 0)
                    ? 0
                    : choose_split_k(*dev, (M + 127) / 128, N, (K + 63) / 64);
+    return MMACT_OK;
+}
+
+MMACT_EXPORT mmact_status mmact_gemm_kernel_choice(int64_t M, int64_t N, int64_t K, int has_residual,
+                                                   int *kernel)
+{
+    if (kernel == nullptr || M < 0 || N < 0 || K < 0) return MMACT_ERR_INVALID_ARG;
+    DeviceInfo *dev = nullptr;
+    mmact_status st = device_info(&dev);
+    if (st != MMACT_OK) return st;
+    if (M == 0 || N == 0 || K == 0) {
+        *kernel = MMACT_GEMM_KERNEL_NONE;
+    } else if (choose_split_k(*dev, (M + 127) / 128, N, (K + 63) / 64) != 0) {
+        *kernel = MMACT_GEMM_KERNEL_SPLIT_K;
+    } else {
+        *kernel = choose_pair(*dev, M, N, (K + 63) / 64, has_residual != 0) ? MMACT_GEMM_KERNEL_PAIR
+                                                                            : MMACT_GEMM_KERNEL_PERSISTENT;
+    }
+    return MMACT_OK;
+}
+
+MMACT_EXPORT mmact_status mmact_set_gemm_pair(int mode)
+{
+    if (mode != 0 && mode != 1 && mode != 2) return MMACT_ERR_INVALID_ARG;
+    g_pair.store(mode);
     return MMACT_OK;
 }
 

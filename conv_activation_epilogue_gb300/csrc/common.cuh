@@ -14,7 +14,7 @@ enum : int { ACT_NONE = 0, ACT_RELU = 1, ACT_LEAKY = 2, ACT_TANH = 3, ACT_SIGMOI
 enum : int { OUT_F32 = 0, OUT_F16 = 1, OUT_BF16 = 2 };
 
 // Bits of the per-device status word.
-enum : unsigned { ST_TIMEOUT = 1u, ST_SMEM_ALIGN = 2u };
+enum : unsigned { ST_TIMEOUT = 1u, ST_SMEM_ALIGN = 2u, ST_PAIR_TMEM = 4u };
 
 constexpr uint64_t DRAIN_NS = 1000000000ull;   // bound on end-of-kernel drains
 

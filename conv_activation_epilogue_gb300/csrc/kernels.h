@@ -27,6 +27,7 @@ struct GemmLaunch {
     int out;             // OUT_*
     int grid;
     int split_k;         // 0: persistent kernel; 2 or 4: split-K cluster kernel (tile_n 256)
+    int pair;            // 1: CTA-pair kernel (256 x 256 tiles over two SMs)
 };
 
 struct ConvArgs {
@@ -114,6 +115,11 @@ cudaError_t setup_splitk_kernels();
 cudaError_t launch_gemm_splitk(const GemmLaunch &L, cudaStream_t stream);
 // Split-K clusters of S CTAs that fit on the device at once (0: unknown).
 int splitk_max_clusters(int S);
+// CTA-pair GEMM: one M = 256 tcgen05.mma per pair of SMs (cta_group::2);
+// args.tiles_m / tiles_n / num_tiles count 256 x 256 pair tiles, grid = 2 x pairs.
+cudaError_t setup_pair_kernels();
+cudaError_t launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream);
+int pair_max_clusters();
 cudaError_t launch_conv(const ConvLaunch &L, cudaStream_t stream);
 // out[i] = act(ws[i]) for i < count (ws fp32, out of dtype `out`).
 cudaError_t launch_act(const float *ws, void *out, int64_t count, int out_kind, int act,

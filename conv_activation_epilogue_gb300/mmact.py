@@ -31,7 +31,7 @@ SYMBOLS = [
     "mmact_conv2d_out_shape", "mmact_conv2d_producer", "mmact_get_last_error",
     "mmact_set_wait_timeout_ns",
     "mmact_selftest_wait_timeout", "mmact_set_gemm_tile_n", "mmact_set_gemm_split_k",
-    "mmact_gemm_split_k_choice", "mmact_status_string", "mmact_version",
+    "mmact_gemm_split_k_choice", "mmact_set_gemm_pair", "mmact_gemm_kernel_choice", "mmact_status_string", "mmact_version",
 ]
 
 
@@ -80,6 +80,8 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     L.mmact_selftest_wait_timeout.argtypes = [u64, vp]
     L.mmact_set_gemm_tile_n.argtypes = [ci]
     L.mmact_set_gemm_split_k.argtypes = [ci]
+    L.mmact_set_gemm_pair.argtypes = [ci]
+    L.mmact_gemm_kernel_choice.argtypes = [i64, i64, i64, ci, ctypes.POINTER(ci)]
     L.mmact_gemm_split_k_choice.argtypes = [i64, i64, i64, ctypes.POINTER(ci)]
     L.mmact_status_string.argtypes = [ci]
     L.mmact_status_string.restype = ctypes.c_char_p
@@ -87,7 +89,7 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     for name in ("mmact_gemm", "mmact_gemm_split", "mmact_conv2d", "mmact_conv2d_split",
                  "mmact_conv2d_out_shape", "mmact_get_last_error", "mmact_selftest_wait_timeout",
                  "mmact_set_gemm_tile_n", "mmact_set_gemm_split_k", "mmact_gemm_split_k_choice",
-                 "mmact_version"):
+                 "mmact_set_gemm_pair", "mmact_gemm_kernel_choice", "mmact_version"):
         getattr(L, name).restype = ci
     _lib = L
     return L
@@ -335,6 +337,22 @@ def mmact_set_gemm_tile_n(tile_n: int) -> None:
 def mmact_set_gemm_split_k(split_k: int) -> None:
     """0: split-K chosen per shape; 1: never; 2 or 4: whenever legal."""
     _check(load().mmact_set_gemm_split_k(int(split_k)), "mmact_set_gemm_split_k")
+
+
+def mmact_set_gemm_pair(mode: int) -> None:
+    """CTA-pair GEMM kernel: 0 chosen per shape; 1 never; 2 always (when split-K is not taken)."""
+    _check(load().mmact_set_gemm_pair(int(mode)), "mmact_set_gemm_pair")
+
+
+GEMM_KERNELS = {0: "none", 1: "persistent", 2: "pair", 3: "split_k"}
+
+
+def mmact_gemm_kernel_choice(M: int, N: int, K: int, residual: bool = False) -> str:
+    """The kernel a GEMM of this shape would run: "none", "persistent", "pair" or "split_k"."""
+    out = ctypes.c_int(-1)
+    _check(load().mmact_gemm_kernel_choice(int(M), int(N), int(K), 1 if residual else 0,
+                                           ctypes.byref(out)), "mmact_gemm_kernel_choice")
+    return GEMM_KERNELS[out.value]
 
 
 def mmact_gemm_split_k_choice(M: int, N: int, K: int) -> int:

@@ -328,6 +328,35 @@ mmact_status mmact_set_gemm_tile_n(int tile_n);
 mmact_status mmact_set_gemm_split_k(int split_k);
 
 /*
+ * Tuning and testing aid: the CTA-pair GEMM kernel, which runs 256 x 256
+ * output tiles on two SMs with one M = 256 tcgen05.mma per pair
+ * (cta_group::2), each SM holding half of A and half of B.  mode: 0 = chosen
+ * per shape (the default: when the persistent kernel would use 256-wide
+ * tiles and the pair grid needs no more waves), 1 = never, 2 = for every
+ * mmact_gemm-family call that does not take the split-K kernel.  Applies to later calls in the
+ * process.  Returns MMACT_ERR_INVALID_ARG for other values.
+ */
+mmact_status mmact_set_gemm_pair(int mode);
+
+/* The GEMM kernels an mmact_gemm-family call can run. */
+typedef enum {
+    MMACT_GEMM_KERNEL_NONE = 0,        /* empty output or K = 0: the bias/activation fill only */
+    MMACT_GEMM_KERNEL_PERSISTENT = 1,  /* one SM per 128 x BN tile, persistent grid */
+    MMACT_GEMM_KERNEL_PAIR = 2,        /* 256 x 256 tiles on CTA pairs (cta_group::2) */
+    MMACT_GEMM_KERNEL_SPLIT_K = 3      /* 128 x 256 tiles on clusters of 2 or 4 CTAs, K split */
+} mmact_gemm_kernel;
+
+/*
+ * Which kernel an mmact_gemm-family call of this shape on the current device
+ * would run (an mmact_gemm_kernel value in *kernel), under the current
+ * settings of mmact_set_gemm_split_k, mmact_set_gemm_pair and
+ * mmact_set_gemm_tile_n; has_residual != 0 for mmact_gemm_residual.  Returns
+ * MMACT_ERR_INVALID_ARG for a null kernel or a negative extent,
+ * MMACT_ERR_CUDA when the device cannot be queried.
+ */
+mmact_status mmact_gemm_kernel_choice(int64_t M, int64_t N, int64_t K, int has_residual, int *kernel);
+
+/*
  * The split-K factor (0 = none, 2 or 4) that an mmact_gemm-family call of
  * this shape on the current device would use under the current setting of
  * mmact_set_gemm_split_k and mmact_set_gemm_tile_n.  Writes it to *split_k.
