@@ -427,6 +427,8 @@ def main():
     ap.add_argument("--no-sustained", action="store_true")
     ap.add_argument("--layout", default="nchw", choices=["nchw", "nhwc"],
                     help="conv workloads: time the channels-last kernel (same values, transposed)")
+    ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "persistent"],
+                    help="GEMM workloads: the planner's kernel, or the one-SM persistent kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -445,6 +447,9 @@ def main():
         dist.init_process_group("nccl", device_id=device)
     build.build()
     mmact.load()
+    if args.gemm_kernel == "persistent":
+        mmact.mmact_set_gemm_pair(1)
+        mmact.mmact_set_gemm_split_k(1)
 
     def barrier():
         if dist is not None:
