@@ -53,6 +53,27 @@ def test_tile_override_validation(lib):
         assert lib.mmact_set_gemm_tile_n(good) == mmact.MMACT_OK
 
 
+def test_kernel_mode_validation(lib):
+    # split-K factor: 0 automatic, 1 never, 2 or 4 forced; pair kernel: 0 automatic, 1 never, 2 forced
+    for bad in (-1, 3, 5, 8):
+        assert lib.mmact_set_gemm_split_k(bad) == mmact.MMACT_ERR_INVALID_ARG
+    for good in (1, 2, 4, 0):
+        assert lib.mmact_set_gemm_split_k(good) == mmact.MMACT_OK
+    for bad in (-1, 3, 4):
+        assert lib.mmact_set_gemm_pair(bad) == mmact.MMACT_ERR_INVALID_ARG
+    for good in (1, 2, 0):
+        assert lib.mmact_set_gemm_pair(good) == mmact.MMACT_OK
+
+
+def test_kernel_choice_queries_reject_bad_arguments(lib):
+    out = ctypes.c_int(-7)
+    assert lib.mmact_gemm_kernel_choice(-1, 8, 8, 0, ctypes.byref(out)) == mmact.MMACT_ERR_INVALID_ARG
+    assert lib.mmact_gemm_kernel_choice(8, 8, 8, 0, None) == mmact.MMACT_ERR_INVALID_ARG
+    assert lib.mmact_gemm_split_k_choice(8, -8, 8, ctypes.byref(out)) == mmact.MMACT_ERR_INVALID_ARG
+    assert lib.mmact_gemm_split_k_choice(8, 8, 8, None) == mmact.MMACT_ERR_INVALID_ARG
+    assert out.value == -7
+
+
 def test_out_shape_matches_oracle(lib):
     orc = oracle.get()
     for (H, W, kh, kw, st, pd, dl) in [(56, 56, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1)),

@@ -80,6 +80,26 @@ def test_pair_kernel_residual(orc):
     check(host(C), orc.gemm(A, B, "bf16", bias, "sigmoid", residual=R, res_dtype="bf16"), "bf16", "pair residual")
 
 
+@pytest.mark.parametrize("cd", ["bf16", "f32"])
+def test_pair_kernel_residual_in_place(orc, cd):
+    # R is C itself: each element is read before its own unit's store writes it
+    rng = np.random.default_rng(21 + len(cd))
+    M, N, K = 512, 512, 512
+    A = rand_codes(rng, (M, K), "bf16")
+    B = rand_codes(rng, (K, N), "bf16")
+    bias = rng.uniform(-1, 1, N).astype(np.float32)
+    if cd == "f32":
+        R = rng.uniform(-1, 1, (M, N)).astype(np.float32)
+        C = fp32_to_device(R).clone()
+    else:
+        R = rand_codes(rng, (M, N), cd)
+        C = to_device(R, cd).clone()
+    mmact.mmact_gemm_residual(to_device(A, "bf16"), to_device(B, "bf16"), fp32_to_device(bias), C, C,
+                              "gelu", 0.0)
+    assert mmact.mmact_get_last_error() == mmact.MMACT_OK
+    check(host(C), orc.gemm(A, B, "bf16", bias, "gelu", residual=R, res_dtype=cd), cd, f"pair in place {cd}")
+
+
 @pytest.mark.parametrize("name", ["gemm_relu_4096x4096x4096_bf16", "gemm_leakyrelu_8192x8192x8192_bf16"])
 def test_pair_kernel_workload(orc, name):
     wl = synth.WORKLOADS[name]
