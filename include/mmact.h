@@ -315,7 +315,8 @@ mmact_status mmact_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
 mmact_status mmact_set_gemm_tile_n(int tile_n);
 
 /*
- * Tuning and testing aid: the split-K GEMM kernel.  For GEMMs with few
+ * Tuning and testing aid (no counterpart in the pages, whose operators split
+ * work over cores by output blocks only): the split-K GEMM kernel.  For GEMMs with few
  * 128 x 256 output tiles (small M) mmact_gemm, mmact_gemm_residual,
  * mmact_gemm_split and mmact_gemm_split_noalloc may run each tile on a
  * thread-block cluster of 2 or 4 CTAs, each CTA accumulating 1/2 or 1/4 of
@@ -328,7 +329,8 @@ mmact_status mmact_set_gemm_tile_n(int tile_n);
 mmact_status mmact_set_gemm_split_k(int split_k);
 
 /*
- * Tuning and testing aid: the CTA-pair GEMM kernel, which runs 256 x 256
+ * Tuning and testing aid (no counterpart in the pages: a GB300 execution
+ * choice for the same operator): the CTA-pair GEMM kernel, which runs 256 x 256
  * output tiles on two SMs with one M = 256 tcgen05.mma per pair
  * (cta_group::2), each SM holding half of A and half of B.  mode: 0 = chosen
  * per shape (the default: when the persistent kernel would use 256-wide
