@@ -183,6 +183,21 @@ def workload_bytes(mmact, wl):
             ob * wl.N * wl.Co * Ho * Wo)
 
 
+def roofline_record(flops, alg_bytes, ms, peaks, peak_src):
+    """The roofline object of the bench line for one launch of `ms` milliseconds: tensor-bound
+    when the workload's arithmetic intensity (algorithmic flops per algorithmic byte) is at or
+    above the ridge point of the two measured peaks, else HBM-bound on algorithmic bytes."""
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if flops / alg_bytes >= ridge:
+        tf = flops / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": tf / peaks["bf16_tflops"], "peak_source": f"{peak_src} burst bf16"}
+    gbs = alg_bytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
+            "alg_bytes_per_launch": alg_bytes}
+
+
 class NhwcProblem:
     """A conv workload in channels-last layout (same values, transposed on the host)."""
 
@@ -527,19 +542,7 @@ def main():
                                                torch_dtype(torch, wl.out_dtype))
         kname = "conv_act_kernel" if producer == "gather" else "conv_vec_kernel"
     in_bytes = prob.input_bytes()
-    # the bound: tensor when the workload's arithmetic intensity (algorithmic flops per
-    # algorithmic byte) is above the ridge point of the two measured peaks, else HBM
-    alg_bytes = workload_bytes(mmact, wl)
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if flops / alg_bytes >= ridge:
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                    "peak_source": f"{peak_src} burst bf16"}
-    else:
-        gbs = alg_bytes / (ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
-                    "alg_bytes_per_launch": alg_bytes}
+    roofline = roofline_record(flops, workload_bytes(mmact, wl), ms, peaks, peak_src)
     roofline["traffic"] = traffic_per_launch(kname, wl.name)
     roofline["kernel"] = kname
 

@@ -1,0 +1,58 @@
+"""Host-side arithmetic of bench.py: algorithmic flops and bytes per workload and the
+roofline object of the bench line (which bound, which peak, which fraction).  No GPU."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from conv_activation_epilogue_gb300 import build, mmact, synth  # noqa: E402
+
+PEAKS = {"bf16_tflops": 1918.4, "hbm_gbs": 6779.7}
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return mmact.load()
+
+
+def test_gemm_flops_and_bytes():
+    wl = synth.WORKLOADS["gemm_leakyrelu_8192x8192x8192_bf16"]
+    assert bench.workload_flops(None, wl) == 2.0 * 8192 ** 3
+    # A and B bf16, bias fp32 [N], C bf16
+    assert bench.workload_bytes(None, wl) == 2.0 * (2 * 8192 * 8192) + 4.0 * 8192 + 2.0 * 8192 * 8192
+    wl = synth.WORKLOADS["matmul_leakyrelu_1024x640x256_f16"]   # fp32 output
+    assert bench.workload_bytes(None, wl) == 2.0 * (1024 * 256 + 256 * 640) + 4.0 * 640 + 4.0 * 1024 * 640
+
+
+def test_conv_flops_and_bytes(lib):
+    wl = synth.WORKLOADS["conv3x3_s2p2d2_tanh_16x128x64x64_bf16"]
+    Ho, Wo = mmact.mmact_conv2d_out_shape(wl.H, wl.W, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation)
+    assert (Ho, Wo) == (32, 32)     # (64 + 2 + 2 - 2 * 2 - 1) // 2 + 1
+    assert bench.workload_flops(mmact, wl) == 2.0 * 16 * 32 * 32 * 256 * 128 * 9
+    assert bench.workload_bytes(mmact, wl) == (2.0 * (16 * 128 * 64 * 64 + 256 * 128 * 9) + 4.0 * 256
+                                              + 2.0 * 16 * 256 * 32 * 32)
+
+
+def test_roofline_bound_follows_the_ridge_point():
+    ridge = PEAKS["bf16_tflops"] * 1e12 / (PEAKS["hbm_gbs"] * 1e9)      # about 283 flop/byte
+    # the square workload is far above the ridge: tensor-bound, fraction of the bf16 peak
+    wl = synth.WORKLOADS["gemm_leakyrelu_8192x8192x8192_bf16"]
+    f, b = bench.workload_flops(None, wl), bench.workload_bytes(None, wl)
+    assert f / b > ridge
+    r = bench.roofline_record(f, b, 0.5731, PEAKS, "measured")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == PEAKS["bf16_tflops"]
+    assert r["achieved"] == pytest.approx(f / 0.5731e-3 / 1e12)
+    assert r["frac"] == pytest.approx(r["achieved"] / PEAKS["bf16_tflops"])
+    # the 128-row workload is below it: HBM-bound on algorithmic bytes
+    wl = synth.WORKLOADS["gemm_leakyrelu_128x8192x8192_bf16"]
+    f, b = bench.workload_flops(None, wl), bench.workload_bytes(None, wl)
+    assert f / b < ridge
+    r = bench.roofline_record(f, b, 0.0300, PEAKS, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == PEAKS["hbm_gbs"]
+    assert r["achieved"] == pytest.approx(b / 0.0300e-3 / 1e9)
+    assert r["alg_bytes_per_launch"] == b
