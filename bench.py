@@ -35,7 +35,7 @@ from conv_activation_epilogue_gb300 import synth  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "fused GEMM/conv+act TFLOP/s and % of GB300 dense bf16 tensor peak (1 GPU)"
-KERNEL_SOURCES = ["common.cuh", "ptx.cuh", "gemm.cu", "gemm_splitk.cu", "gemm_pair.cu", "conv.cu", "conv_vec.cu", "conv_nhwc.cu", "elementwise.cu", "api.cu"]
+KERNEL_SOURCES = ["common.cuh", "ptx.cuh", "gemm.cu", "gemm_splitk.cu", "gemm_pair.cu", "conv.cu", "conv_vec.cu", "conv_nhwc.cu", "conv_tmem.cu", "elementwise.cu", "api.cu"]
 
 
 def env_int(name, default):
@@ -102,8 +102,9 @@ class ClockSampler:
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, period_ms=50):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
         self.lines = []
         self.thread = None
@@ -112,7 +113,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -122,7 +123,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def stop(self):
         if self.proc is None:
@@ -134,9 +135,16 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
+        return self.summary()
+
+    def summary(self, t_from=None, t_to=None):
+        """Median SM clock, max clock and throttle reasons of the samples received in
+        [t_from, t_to] (host perf_counter seconds; all samples by default)."""
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
+            if (t_from is not None and t < t_from) or (t_to is not None and t > t_to):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -173,29 +181,67 @@ def workload_flops(mmact, wl):
     return 2.0 * wl.N * Ho * Wo * wl.Co * wl.C * wl.kh * wl.kw
 
 
+def conv_lines_read(size, k, stride, pad_lo, dil, out):
+    """How many of an input axis's `size` lines some output reads: the distinct
+    o*stride - pad_lo + r*dil (0 <= o < out, 0 <= r < k) inside [0, size)."""
+    return len({o * stride - pad_lo + r * dil for o in range(out) for r in range(k)} & set(range(size)))
+
+
 def workload_bytes(mmact, wl):
-    """Algorithmic HBM bytes: read every input once, write the output once."""
+    """Algorithmic HBM bytes: read every input element the operator needs once, write the output
+    once.  For a conv that counts only the input rows and columns some output reads (a 1x1
+    stride-2 conv reads a quarter of x; so does a 3x3 stride-2 dilation-2 one)."""
     ob = 4 if (wl.c_dtype if wl.kind == "gemm" else wl.out_dtype) == "f32" else 2
     if wl.kind == "gemm":
         return 2.0 * (wl.M * wl.K + wl.K * wl.N) + 4.0 * wl.N + ob * wl.M * wl.N
     Ho, Wo = mmact.mmact_conv2d_out_shape(wl.H, wl.W, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation)
-    return (2.0 * (wl.N * wl.C * wl.H * wl.W + wl.Co * wl.C * wl.kh * wl.kw) + 4.0 * wl.Co +
+    rows = conv_lines_read(wl.H, wl.kh, wl.stride[0], wl.pads[0], wl.dilation[0], Ho)
+    cols = conv_lines_read(wl.W, wl.kw, wl.stride[1], wl.pads[2], wl.dilation[1], Wo)
+    return (2.0 * (wl.N * wl.C * rows * cols + wl.Co * wl.C * wl.kh * wl.kw) + 4.0 * wl.Co +
             ob * wl.N * wl.Co * Ho * Wo)
 
 
-def roofline_record(flops, alg_bytes, ms, peaks, peak_src):
-    """The roofline object of the bench line for one launch of `ms` milliseconds: tensor-bound
-    when the workload's arithmetic intensity (algorithmic flops per algorithmic byte) is at or
-    above the ridge point of the two measured peaks, else HBM-bound on algorithmic bytes."""
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+def roofline_record(flops, alg_bytes, ms, peaks, peak_src, tf32=False):
+    """The roofline object for one launch of `ms` milliseconds: tensor-bound when the workload's
+    arithmetic intensity (algorithmic flops per algorithmic byte) is at or above the ridge point
+    of the two measured peaks, else HBM-bound on algorithmic bytes.  The tensor peak is the
+    measured cuBLAS bf16 burst figure (for tf32 operands half of it, the nominal ratio)."""
+    tpeak = peaks["bf16_tflops"] / (2.0 if tf32 else 1.0)
+    ridge = tpeak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if flops / alg_bytes >= ridge:
         tf = flops / (ms * 1e-3) / 1e12
-        return {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": tf / peaks["bf16_tflops"], "peak_source": f"{peak_src} burst bf16"}
+        return {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s",
+                "frac": tf / tpeak,
+                "peak_source": f"{peak_src} burst bf16" + (" / 2 (tf32)" if tf32 else ""),
+                "alg_bytes_per_launch": alg_bytes}
     gbs = alg_bytes / (ms * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
             "alg_bytes_per_launch": alg_bytes}
+
+
+# Dense bf16 tensor-core rate of one GB300 SM: 8192 flop per clock (one 128 x 256 x 16
+# tcgen05.mma every 128 cycles).  Measured, not quoted: the CTA-pair GEMM ran 1923 TFLOP/s
+# at 1.78 GHz with the tensor pipe busy 86.9 % of elapsed cycles (ncu), i.e. 8180 flop per
+# clock per SM on 152 SMs.  NVIDIA's nominal dense figure for the part is 2.25 PFLOP/s.
+TENSOR_FLOP_PER_CLK_PER_SM = 8192
+NOMINAL_DENSE_BF16_TFLOPS = 2250.0
+
+
+def tensor_capacity(achieved_tflops, sms, sm_mhz, sm_max_mhz):
+    """The achieved rate against the tensor pipes' own capacity: SM count x flop per clock x
+    clock, at the SM clock sampled under this load and at the maximum clock, and against
+    NVIDIA's nominal dense figure."""
+    rec = {"flop_per_clk_per_sm": TENSOR_FLOP_PER_CLK_PER_SM, "sms": sms,
+           "nominal_dense_tflops": NOMINAL_DENSE_BF16_TFLOPS,
+           "frac_of_nominal": achieved_tflops / NOMINAL_DENSE_BF16_TFLOPS}
+    for key, mhz in (("at_sampled_clock", sm_mhz), ("at_max_clock", sm_max_mhz)):
+        if mhz:
+            cap = sms * TENSOR_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12
+            rec[f"peak_tflops_{key}"] = cap
+            rec[f"frac_{key}"] = achieved_tflops / cap
+    rec["sm_mhz"] = sm_mhz
+    return rec
 
 
 class NhwcProblem:
@@ -479,49 +525,59 @@ def main():
     stream = torch.cuda.current_stream()
 
     # --- timed region: K fused launches, inputs resident, > L2 so no flush needed
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
     for _ in range(args.warmup):
         prob.run("fused")
+    w1.record(stream)
     torch.cuda.synchronize()
+    est_ms = w0.elapsed_time(w1) / args.warmup      # sizes the sustained leg below
     st = mmact.mmact_get_last_error()
     if st != mmact.MMACT_OK:
         raise RuntimeError(f"kernel status {mmact.mmact_status_string(st)}")
+    # One clock sampler runs through the timed region and the sustained leg that follows it
+    # with no gap: the K timed steps last milliseconds, shorter than nvidia-smi's sampling
+    # period, so the clock the launch ran at is read over the whole back-to-back window.
     clocks = ClockSampler(local)
     barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_load0 = time.perf_counter()
     start.record(stream)
     for _ in range(args.steps):
         prob.run("fused")
     end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    clock_rec = clocks.stop()
-    ms = reduce_max(dist, start.elapsed_time(end) / args.steps, device)
-    st = mmact.mmact_get_last_error()
-    if st != mmact.MMACT_OK:
-        raise RuntimeError(f"kernel status {mmact.mmact_status_string(st)}")
-
-    # --- sustained: the same launch back to back for ~2 s, clocks sampled throughout
+    # --- sustained: the same launch back to back for ~2 s right after the timed steps
     sustained = None
-    if rank == 0 and not args.no_sustained:
-        n_sus = max(args.steps, int(2.0 / (ms * 1e-3)))
-        sampler = ClockSampler(local)
-        sampler.start()
-        time.sleep(0.2)
+    s0 = s1 = None
+    n_sus = 0
+    if not args.no_sustained:
+        n_sus = max(args.steps, int(2.0 / (max(est_ms, 1e-3) * 1e-3)))
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record(stream)
         for _ in range(n_sus):
             prob.run("fused")
         s1.record(stream)
-        torch.cuda.synchronize()
-        sus_clocks = sampler.stop()
+    torch.cuda.synchronize()
+    t_load1 = time.perf_counter()
+    barrier()
+    clocks.stop()
+    clock_rec = clocks.summary(t_load0, t_load1)
+    if clock_rec is not None:
+        clock_rec["window"] = ("the timed steps and the ~2 s of the same launch that follow them back to back"
+                               if s0 is not None else "the timed steps")
+    ms = reduce_max(dist, start.elapsed_time(end) / args.steps, device)
+    st = mmact.mmact_get_last_error()
+    if st != mmact.MMACT_OK:
+        raise RuntimeError(f"kernel status {mmact.mmact_status_string(st)}")
+    if s0 is not None and rank == 0:
         sus_ms = s0.elapsed_time(s1) / n_sus
         sus_tf = flops / (sus_ms * 1e-3) / 1e12
         sustained = {"launches": n_sus, "seconds": round(sus_ms * n_sus / 1e3, 2),
                      "ms_per_step": sus_ms, "tflops": sus_tf,
-                     "frac_of_sustained_peak": None, "clocks": sus_clocks}
+                     "frac_of_sustained_peak": None, "clocks": clock_rec}
 
     import oracle as oracle_mod
     parity = parity_spot_check(oracle_mod, prob) if rank == 0 else None
@@ -540,11 +596,14 @@ def main():
         producer = mmact.mmact_conv2d_producer(wl.N, wl.C, wl.H, wl.W, wl.Co, wl.kh, wl.kw, wl.stride,
                                                wl.pads, wl.dilation, torch_dtype(torch, wl.dtype),
                                                torch_dtype(torch, wl.out_dtype))
-        kname = "conv_act_kernel" if producer == "gather" else "conv_vec_kernel"
+        kname = {"gather": "conv_act_kernel", "tmem": "conv_tmem_kernel"}.get(producer, "conv_vec_kernel")
     in_bytes = prob.input_bytes()
     roofline = roofline_record(flops, workload_bytes(mmact, wl), ms, peaks, peak_src)
     roofline["traffic"] = traffic_per_launch(kname, wl.name)
     roofline["kernel"] = kname
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    capacity = tensor_capacity(achieved, sms, clock_rec["sm_mhz"] if clock_rec else None,
+                               clock_rec["sm_max_mhz"] if clock_rec else None)
 
     # --- end to end through the public API with host buffers
     e2e = None
@@ -564,6 +623,7 @@ def main():
                    "pct_of_bf16_peak": round(100.0 * achieved / peaks["bf16_tflops"], 2)},
         "gpu_launches": args.steps,
         "roofline": roofline,
+        "tensor_capacity": capacity,
         "parity_max_err_over_bound": parity,
         "clocks": clock_rec,
         "sustained": sustained,
@@ -652,9 +712,58 @@ def end_to_end(torch, mmact, wl, prob, device, stream, args, flops, world, barri
         raise RuntimeError(f"kernel status {mmact.mmact_status_string(st)}")
     h2d = sum(t.numel() * t.element_size() for t in hosts)
     d2h = houts[0].numel() * houts[0].element_size()
+    link = host_link(torch, hosts, devs[0], houts[0], prob.out, s_up, s_down)
+    link["e2e_floor_ms"] = (h2d / (link["h2d_gbs"] * 1e9) if link["h2d_gbs"] else 0.0) * 1e3
+    link["concurrent_floor_ms"] = ((h2d + d2h) / (link["concurrent_gbs"] * 1e9)) * 1e3
     return {"value": job_tflops(flops, ms, world), "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
-            "pipelining": "upload / compute / download on three streams, two buffer sets"}
+            "pipelining": "upload / compute / download on three streams, two buffer sets",
+            "host_link": link}
+
+
+def host_link(torch, hosts, devs, hout, dout, s_up, s_down, reps=6):
+    """Plain pinned-memory copies of one step's bytes, no kernel: host -> device alone,
+    device -> host alone, and both at once on two streams (GB/s, CUDA events).  The
+    pipelined end-to-end step cannot be faster than its copies at these rates."""
+    def timed(fn, streams):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(streams[0])
+        for st in streams[1:]:
+            st.wait_event(e0)
+        for _ in range(reps):
+            fn()
+        for st in streams[1:]:
+            ev = torch.cuda.Event()
+            ev.record(st)
+            streams[0].wait_event(ev)
+        e1.record(streams[0])
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    h2d_bytes = sum(t.numel() * t.element_size() for t in hosts)
+    d2h_bytes = hout.numel() * hout.element_size()
+
+    def up():
+        with torch.cuda.stream(s_up):
+            for src, dst in zip(hosts, devs):
+                dst.copy_(src, non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(s_down):
+            hout.copy_(dout, non_blocking=True)
+
+    def both():
+        up()
+        down()
+
+    ms_up = timed(up, [s_up])
+    ms_down = timed(down, [s_down])
+    ms_both = timed(both, [s_up, s_down])
+    return {"h2d_gbs": h2d_bytes / (ms_up * 1e-3) / 1e9, "d2h_gbs": d2h_bytes / (ms_down * 1e-3) / 1e9,
+            "concurrent_gbs": (h2d_bytes + d2h_bytes) / (ms_both * 1e-3) / 1e9,
+            "what": "pinned host buffers, one step's inputs up and its output down, no kernel"}
 
 
 def sweep(torch, mmact, device, stream, peaks):
@@ -666,13 +775,19 @@ def sweep(torch, mmact, device, stream, peaks):
         nbytes = workload_bytes(mmact, wl)
         rec = {"timing": "CUDA graph of 20 back-to-back calls, replayed 3 times"}
         variants = ("fused", "split") + (("fused_residual",) if wl.kind == "gemm" else ())
+        def row(ms, nb=nbytes, tf32=False):
+            tf = flops / (ms * 1e-3) / 1e12
+            rl = roofline_record(flops, nb, ms, peaks, "measured", tf32=tf32)
+            return {"ms": round(ms, 5), "tflops": round(tf, 2),
+                    "pct_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 2),
+                    "alg_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
+                    "roofline": {"bound": rl["bound"], "achieved": round(rl["achieved"], 2),
+                                 "peak": rl["peak"], "unit": rl["unit"], "frac": round(rl["frac"], 4)}}
+
         for variant in variants:
             ms = time_graph(torch, lambda: prob.run(variant), 20, stream)
-            tf = flops / (ms * 1e-3) / 1e12
             nb = nbytes + (prob.out.numel() * prob.out.element_size() if variant == "fused_residual" else 0)
-            rec[variant] = {"ms": round(ms, 5), "tflops": round(tf, 2),
-                            "pct_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 2),
-                            "alg_gbs": round(nb / (ms * 1e-3) / 1e9, 1)}
+            rec[variant] = row(ms, nb)
         # the fused-vs-split decision, re-measured on every run
         rec["fused_speedup_over_split"] = round(rec["split"]["ms"] / rec["fused"]["ms"], 3)
         if wl.kind == "gemm":
@@ -688,29 +803,32 @@ def sweep(torch, mmact, device, stream, peaks):
                 finally:
                     mmact.mmact_set_gemm_split_k(0)
                     mmact.mmact_set_gemm_pair(0)
-                tf = flops / (ms * 1e-3) / 1e12
-                rec["fused_persistent_kernel"] = {"ms": round(ms, 5), "tflops": round(tf, 2),
-                                                  "pct_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 2),
-                                                  "alg_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+                rec["fused_persistent_kernel"] = row(ms)
         if wl.kind == "conv":
             rec["nchw_producer"] = mmact.mmact_conv2d_producer(
                 wl.N, wl.C, wl.H, wl.W, wl.Co, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation,
                 torch_dtype(torch, wl.dtype), torch_dtype(torch, wl.out_dtype))
+            # the same NCHW call with the tensor-memory im2col kernel turned off (window /
+            # vector producers), beside the planner's choice
+            mmact.mmact_set_conv_tmem(1)
+            try:
+                rec["nchw_legacy_producer"] = mmact.mmact_conv2d_producer(
+                    wl.N, wl.C, wl.H, wl.W, wl.Co, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation,
+                    torch_dtype(torch, wl.dtype), torch_dtype(torch, wl.out_dtype))
+                rec["fused_legacy_producer"] = row(time_graph(torch, lambda: prob.run("fused"), 20, stream))
+            finally:
+                mmact.mmact_set_conv_tmem(0)
         if wl.kind == "conv":
             # the same convolution on channels-last tensors (x NHWC, w [Co,kh,kw,C], y NHWC)
             nprob = NhwcProblem(torch, mmact, wl, device, inputs=prob.host)
-            ms = time_graph(torch, lambda: nprob.run(), 20, stream)
-            tf = flops / (ms * 1e-3) / 1e12
-            rec["fused_nhwc"] = {"ms": round(ms, 5), "tflops": round(tf, 2),
-                                 "pct_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 2),
-                                 "alg_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+            rec["fused_nhwc"] = row(time_graph(torch, lambda: nprob.run(), 20, stream))
             del nprob
             # fp32 inputs (same values), tf32 tensor-core arithmetic; peak: nominal tf32 = bf16 / 2
             fprob = NhwcProblem(torch, mmact, wl, device, inputs=prob.host, fp32_inputs=True)
             ms = time_graph(torch, lambda: fprob.run(), 20, stream)
-            tf = flops / (ms * 1e-3) / 1e12
-            rec["fused_nhwc_fp32_inputs"] = {"ms": round(ms, 5), "tflops": round(tf, 2),
-                                             "pct_tf32_peak": round(200 * tf / peaks["bf16_tflops"], 2)}
+            # fp32 inputs double the input bytes
+            x_w = nbytes - 4.0 * wl.Co - (4 if wl.out_dtype == "f32" else 2) * prob.out.numel()
+            rec["fused_nhwc_fp32_inputs"] = row(ms, nbytes + x_w, tf32=True)
             del fprob
         st = mmact.mmact_get_last_error()
         rec["status"] = mmact.mmact_status_string(st)

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libmmact.so")
-SOURCES = ["api.cu", "gemm.cu", "gemm_splitk.cu", "gemm_pair.cu", "conv.cu", "conv_vec.cu", "conv_nhwc.cu", "elementwise.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "gemm.cu", "gemm_splitk.cu", "gemm_pair.cu", "conv.cu", "conv_vec.cu", "conv_nhwc.cu", "conv_tmem.cu", "elementwise.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -6,6 +6,7 @@
 // validation (an invalid value is rejected with the supported set named,
 // before anything runs): every check here happens before any launch, and a
 // failed check enqueues nothing.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -30,6 +31,7 @@ std::atomic<uint64_t> g_wait_ns{DEFAULT_WAIT_NS};
 std::atomic<int> g_tile_n{0};
 std::atomic<int> g_split_k{0};   // 0: chosen per shape; 1: never; 2 or 4: whenever legal
 std::atomic<int> g_pair{0};      // CTA-pair GEMM kernel: 0 chosen per shape; 1 never; 2 always
+std::atomic<int> g_conv_tmem{0}; // NCHW conv, im2col operand in TMEM: 0 when supported; 1 never
 
 constexpr int MAX_DEVICES = 64;
 struct DeviceInfo {
@@ -61,7 +63,8 @@ mmact_status device_info(DeviceInfo **out)
             return MMACT_ERR_CUDA;
         if (setup_gemm_kernels() != cudaSuccess || setup_conv_kernels() != cudaSuccess ||
             setup_conv_vec_kernels() != cudaSuccess || setup_nhwc_kernels() != cudaSuccess ||
-            setup_splitk_kernels() != cudaSuccess || setup_pair_kernels() != cudaSuccess)
+            setup_splitk_kernels() != cudaSuccess || setup_pair_kernels() != cudaSuccess ||
+            setup_conv_tmem_kernels() != cudaSuccess)
             return MMACT_ERR_CUDA;
         d.pair_clusters = pair_max_clusters();
         d.splitk_clusters[0] = splitk_max_clusters(2);
@@ -273,21 +276,6 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
     return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
 }
 
-mmact_status gemm_check(const void *A, const void *B, const float *bias, const void *C, int64_t M,
-                        int64_t N, int64_t K, mmact_dtype ab, mmact_dtype cd, mmact_act act)
-{
-    if (M < 0 || N < 0 || K < 0 || M > MAX_DIM || N > MAX_DIM || K > MAX_DIM)
-        return MMACT_ERR_INVALID_ARG;
-    // a pointer may be null only when its tensor is empty
-    if ((A == nullptr && M * K != 0) || (B == nullptr && K * N != 0) || (C == nullptr && M * N != 0))
-        return MMACT_ERR_INVALID_ARG;
-    if (!valid_in(ab) || !valid_out(cd) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
-    if (bias != nullptr && !aligned4(bias)) return MMACT_ERR_INVALID_ARG;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return MMACT_ERR_UNSUPPORTED;
-    if (K % 8 != 0 || N % 8 != 0) return MMACT_ERR_UNSUPPORTED;
-    return MMACT_OK;
-}
-
 struct ConvGeom {
     int64_t Ho, Wo;
 };
@@ -410,6 +398,135 @@ void conv_plan(int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t k
     }
 }
 
+int64_t gcd64(int64_t a, int64_t b)
+{
+    while (b != 0) {
+        const int64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+// Plan of the NCHW conv kernel whose im2col operand lives in tensor memory
+// (conv_tmem.cu): tiles of 128 consecutive output pixels of one image x BN
+// output channels; per 64-value K block one raw input window box.  Returns
+// false when the geometry needs another kernel: 16-bit inputs, filter rows
+// and input rows with 16-byte pitches (K % 8, W % 8), a window that fits its
+// slot and the TMA box limits, and a K-offset table that fits.
+bool tconv_plan(int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
+                const int32_t *st, const int32_t *pd, const int32_t *dl, const ConvGeom &g,
+                mmact_dtype in, TmemConvArgs &a, int &bn)
+{
+    std::memset(&a, 0, sizeof(a));
+    if (!valid_in(in)) return false;
+    const int64_t taps = kh * kw, K = C * taps, P = g.Ho * g.Wo;
+    if (K % 8 != 0 || W % 8 != 0 || P <= 0) return false;
+    const int64_t period = taps / gcd64(64, taps);          // blocks until the K pattern repeats
+    if (period * 64 > CONV_TMEM_TABLE_MAX) return false;
+    // output rows a 128-pixel tile can span (tiles start at multiples of 128)
+    const int64_t tiles_p = (P + 127) / 128;
+    int64_t nrows = 1;
+    const int64_t starts = std::min<int64_t>(g.Wo / gcd64(128, g.Wo), tiles_p);
+    for (int64_t i = 0; i < starts; ++i) {
+        const int64_t s = (128 * i) % g.Wo;
+        nrows = std::max<int64_t>(nrows, (s + 127) / g.Wo + 1);
+    }
+    nrows = std::min<int64_t>(nrows, g.Ho);
+    const int64_t sh = st[0], sw = st[1], dh = dl[0], dw = dl[1];
+    const bool lattice = sh > 1 && (kh == 1 || dh % sh == 0);
+    const int64_t HB = lattice ? nrows + (kh - 1) * (dh / sh) : (nrows - 1) * sh + (kh - 1) * dh + 1;
+    const int64_t esh = lattice ? sh : 1;
+    const int64_t x0 = -(((int64_t)pd[2] + 7) / 8) * 8;
+    const int64_t xoff = -(int64_t)pd[2] - x0;
+    const int64_t WB = ((xoff + (g.Wo - 1) * sw + (kw - 1) * dw + 1) + 7) / 8 * 8;
+    const int64_t CB = (64 % taps == 0) ? 64 / taps : 63 / taps + 2;
+    const int64_t raw = WB * HB * CB * 2;
+    if (raw > CONV_TMEM_WIN_MAX_BYTES || WB > 256 || HB * esh > 256 || CB > 256) return false;
+    bn = Co <= 64 ? 64 : (Co <= 128 ? 128 : 256);
+    // window ring: as many 1 KB-rounded slots as the kernel's shared memory leaves, up to 8
+    const int64_t slot = (raw + 1023) / 1024 * 1024;
+    const int64_t wstages = std::min<int64_t>(CONV_TMEM_MAX_WSTAGES, conv_tmem_window_region(bn) / slot);
+    if (wstages < 2) return false;
+    a.Nb = (int)N;
+    a.C = (int)C;
+    a.H = (int)H;
+    a.W = (int)W;
+    a.Co = (int)Co;
+    a.kh = (int)kh;
+    a.kw = (int)kw;
+    a.sh = (int)sh;
+    a.sw = (int)sw;
+    a.pt = pd[0];
+    a.pl = pd[2];
+    a.dh = (int)dh;
+    a.dw = (int)dw;
+    a.Ho = (int)g.Ho;
+    a.Wo = (int)g.Wo;
+    a.P = (int)P;
+    a.K = (int)K;
+    a.tiles_co = (int)((Co + bn - 1) / bn);
+    a.tiles_p = (int)tiles_p;
+    if (N * a.tiles_co * tiles_p > MAX_DIM) return false;
+    a.num_tiles = (int)(N * a.tiles_co * tiles_p);
+    a.num_kb = (int)((K + 63) / 64);
+    a.ab_bf16 = in == MMACT_BF16 ? 1 : 0;
+    a.WB = (int)WB;
+    a.HB = (int)HB;
+    a.CB = (int)CB;
+    a.esh = (int)esh;
+    a.rowmul = lattice ? 1 : (int)sh;
+    a.rstep = lattice ? (int)(dh / sh) : (int)dh;
+    a.x0 = (int)x0;
+    a.xoff = (int)xoff;
+    a.raw_bytes = (int)raw;
+    a.win_slot = (int)slot;
+    a.wstages = (int)wstages;
+    a.tab_period = (int)period;
+    return true;
+}
+
+bool use_tconv() { return g_conv_tmem.load() == 0; }
+
+mmact_status tconv_enqueue(const void *x, const void *w, const float *bias, void *y, int64_t N, int64_t C,
+                           int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
+                           const TmemConvArgs &plan, int bn, const DeviceInfo *dev, mmact_dtype in,
+                           mmact_dtype out, mmact_act act, float alpha, cudaStream_t stream, const void *res)
+{
+    TmemConvLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    L.args = plan;
+    TmemConvArgs &a = L.args;
+    a.act = (int)act;
+    a.alpha = alpha;
+    a.bias = bias;
+    a.res = res;
+    a.y = y;
+    a.status = dev->status;
+    a.wait_ns = g_wait_ns.load();
+    L.tile_n = bn;
+    L.out = out_kind(out);
+    L.grid = (int)std::min<int64_t>(a.num_tiles, dev->sm_count);
+    const int e = elem_bytes(out);
+    a.y_tma = ((int64_t)a.P * e) % 16 == 0 ? 1 : 0;
+    const uint64_t dW[2] = {(uint64_t)a.K, (uint64_t)Co}, sW[1] = {(uint64_t)a.K * 2};
+    const uint32_t bW[2] = {64, (uint32_t)bn};
+    const uint64_t dX[4] = {(uint64_t)W, (uint64_t)H, (uint64_t)C, (uint64_t)N};
+    const uint64_t sX[3] = {(uint64_t)W * 2, (uint64_t)H * W * 2, (uint64_t)C * H * W * 2};
+    const uint32_t bX[4] = {(uint32_t)a.WB, (uint32_t)(a.HB * a.esh), (uint32_t)a.CB, 1};
+    const uint32_t eX[4] = {1, (uint32_t)a.esh, 1, 1};
+    if (!encode(&L.tmW, in, 2, w, dW, sW, bW) || !encode(&L.tmX, in, 4, x, dX, sX, bX, false, eX))
+        return MMACT_ERR_CUDA;
+    if (a.y_tma) {
+        // y as {P, Co, N}: 32 pixels x 32 channels per store, unswizzled [channel][pixel] rows
+        const uint64_t dY[3] = {(uint64_t)a.P, (uint64_t)Co, (uint64_t)N};
+        const uint64_t sY[2] = {(uint64_t)a.P * e, (uint64_t)Co * a.P * e};
+        const uint32_t bY[3] = {32, 32, 1};
+        if (!encode(&L.tmY, out, 3, y, dY, sY, bY, false)) return MMACT_ERR_CUDA;
+    }
+    return launch_conv_tmem(L, stream) == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
+}
+
 mmact_status conv_enqueue(const void *x, const void *w, const float *bias, void *y, int64_t N,
                           int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
                           const int32_t *st, const int32_t *pd, const int32_t *dl, const ConvGeom &g,
@@ -425,6 +542,13 @@ mmact_status conv_enqueue(const void *x, const void *w, const float *bias, void 
         cudaError_t e = launch_bias_act(bias, y, N * Co, P, 1, Co, out_kind(out), (int)act, alpha, stream,
                                         res);
         return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
+    }
+    if (use_tconv()) {
+        TmemConvArgs tp;
+        int bn = 0;
+        if (tconv_plan(N, C, H, W, Co, kh, kw, st, pd, dl, g, in, tp, bn))
+            return tconv_enqueue(x, w, bias, y, N, C, H, W, Co, kh, kw, tp, bn, dev, in, out, act, alpha,
+                                 stream, res);
     }
     ConvLaunch L;
     std::memset(&L, 0, sizeof(L));
@@ -578,6 +702,24 @@ mmact_status residual_check(const void *R, const void *out, int64_t bytes)
 }
 
 }  // namespace
+
+// Host validation shared by every mmact_gemm-family entry point (also used by
+// the no-allocation entry point in noalloc.cu, before its own size limit).
+mmact_status gemm_check(const void *A, const void *B, const float *bias, const void *C, int64_t M,
+                        int64_t N, int64_t K, mmact_dtype ab, mmact_dtype cd, mmact_act act)
+{
+    if (M < 0 || N < 0 || K < 0 || M > MAX_DIM || N > MAX_DIM || K > MAX_DIM)
+        return MMACT_ERR_INVALID_ARG;
+    // a pointer may be null only when its tensor is empty
+    if ((A == nullptr && M * K != 0) || (B == nullptr && K * N != 0) || (C == nullptr && M * N != 0))
+        return MMACT_ERR_INVALID_ARG;
+    if (!valid_in(ab) || !valid_out(cd) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
+    if (bias != nullptr && !aligned4(bias)) return MMACT_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return MMACT_ERR_UNSUPPORTED;
+    if (K % 8 != 0 || N % 8 != 0) return MMACT_ERR_UNSUPPORTED;
+    return MMACT_OK;
+}
+
 }  // namespace mmact
 
 using namespace mmact;
@@ -753,6 +895,12 @@ MMACT_EXPORT int mmact_conv2d_producer(int64_t N, int64_t C, int64_t H, int64_t 
     if (N < 0 || C <= 0 || Co < 0 || !valid_in(in_dtype) || !valid_out(out_dtype)) return -1;
     if (conv_geom(H, W, kh, kw, strides, pads, dilations, &g) != MMACT_OK) return -1;
     if (C * H * W > MAX_DIM || Co * g.Ho * g.Wo > MAX_DIM || C * kh * kw > MAX_DIM) return -1;
+    if (use_tconv()) {
+        TmemConvArgs tp;
+        int bn = 0;
+        if (tconv_plan(N, C, H, W, Co, kh, kw, strides, pads, dilations, g, in_dtype, tp, bn))
+            return MMACT_CONV_TMEM;
+    }
     ConvArgs a;
     conv_plan(N, C, H, W, Co, kh, kw, strides, pads, dilations, g, in_dtype, out_dtype, a);
     return a.win ? MMACT_CONV_WINDOW : a.vec ? MMACT_CONV_VECTOR : MMACT_CONV_GATHER;
@@ -833,6 +981,13 @@ MMACT_EXPORT mmact_status mmact_set_gemm_pair(int mode)
 {
     if (mode != 0 && mode != 1 && mode != 2) return MMACT_ERR_INVALID_ARG;
     g_pair.store(mode);
+    return MMACT_OK;
+}
+
+MMACT_EXPORT mmact_status mmact_set_conv_tmem(int mode)
+{
+    if (mode != 0 && mode != 1) return MMACT_ERR_INVALID_ARG;
+    g_conv_tmem.store(mode);
     return MMACT_OK;
 }
 

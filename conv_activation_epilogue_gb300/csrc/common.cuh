@@ -113,6 +113,19 @@ __device__ __forceinline__ bool pipe_wait(const Pipe &pp, uint32_t bar, uint32_t
     return ptx::mbar_wait_bounded(bar, parity, pp.wait_ns, pp.abort, PIPE_SUSPEND_NS);
 }
 
+// Spinning variant for waits on the critical path whose phase is completed
+// by thread arrivals (no suspend hint: the waiting thread re-polls).
+__device__ __forceinline__ bool pipe_wait_spin(const Pipe &pp, uint32_t bar, uint32_t parity)
+{
+    return ptx::mbar_wait_bounded(bar, parity, pp.wait_ns, pp.abort, 0);
+}
+
+__device__ __forceinline__ bool warp_pipe_wait_spin(const Pipe &pp, uint32_t bar, uint32_t parity)
+{
+    const uint32_t r = pipe_wait_spin(pp, bar, parity) ? 1u : 0u;
+    return __shfl_sync(0xffffffffu, r, 0) != 0u;
+}
+
 // The epilogue's wait for a finished accumulator: long, and not on the
 // critical path, so the waiting warps are parked between polls.
 __device__ __forceinline__ bool epi_wait(const Pipe &pp, uint32_t bar, uint32_t parity)
@@ -169,9 +182,14 @@ struct TileN {
 // that makes the stores visible to the tensor core's operand reads.
 // TF32: the operands are fp32 (kind::tf32, 8 K per instruction = 32 bytes,
 // the same K step as the 16-bit kinds; both operands must be K-major).
+// last_bar (optional, 0 = none): an mbarrier of count 1 that also receives the
+// commit of the CTA's last tile, so that warps which only help with that
+// tile's epilogue can wait for it by phase 0 (a parity wait on the
+// accumulator barrier alone could match an earlier tile's phase when those
+// warps run far ahead of the MMAs).
 template <int BN, int STAGES, bool B_KMAJOR = false, bool THREAD_FILLED = false, bool TF32 = false>
 __device__ void mma_role(const Pipe &pp, uint32_t sA, uint32_t sB, int num_tiles, int num_kb,
-                         uint32_t idesc)
+                         uint32_t idesc, uint32_t last_bar = 0)
 {
     constexpr uint32_t A_BYTES = 128 * 64 * 2;
     constexpr uint32_t B_BYTES = B_KMAJOR ? (uint32_t)BN * 128u : TileN<BN>::B_BYTES;
@@ -199,6 +217,7 @@ __device__ void mma_role(const Pipe &pp, uint32_t sA, uint32_t sB, int num_tiles
         }
         if (!ok) break;
         ptx::mma_commit(pp.tfull0 + 8 * acc);
+        if (last_bar != 0 && t + (int)gridDim.x >= num_tiles) ptx::mma_commit(last_bar);
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
     }

@@ -54,7 +54,7 @@ struct ConvVecCfg {
     static constexpr int OFF_RAW = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_EPI = OFF_RAW + RSTAGES * RAW_MAX;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * RSTAGES;
+    static constexpr int NUM_BARS = 2 * STAGES + 6 + 2 * RSTAGES;   // + the last tile's accumulator
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int GATHER_WARPS = 8;
@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
     pp.wait_ns = p.wait_ns;
     const uint32_t rfull0 = pp.drain + 8;                // input-window ring (WIN)
     const uint32_t rempty0 = rfull0 + 8 * Cfg::RSTAGES;
+    const uint32_t tlast = rempty0 + 8 * Cfg::RSTAGES;   // the CTA's last accumulator is complete
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
             ptx::mbar_init(pp.tempty0 + 8 * a, 4);
         }
         ptx::mbar_init(pp.drain, 1);
+        ptx::mbar_init(tlast, 1);
         misc[1] = 0;
         ptx::fence_mbar_init();
     }
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0)
             mma_role<BN, STAGES, false, true>(pp, sA, sB, p.num_tiles, p.num_kb,
-                                              ptx::idesc_f16(p.ab_bf16 != 0, false, true, 128, BN));
+                                              ptx::idesc_f16(p.ab_bf16 != 0, false, true, 128, BN), tlast);
     } else if (warp >= 6 && WIN) {
         // ------------------------------------ B-tile build from the window --
         // Same lane -> (tile row, 8-pixel vector) mapping and B-tile
@@ -375,16 +377,16 @@ __global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
             // ------------------------------- help with the last tile's epilogue --
             // Gather warp g (lane quarter g & 3) takes units u = 1 + (g >> 2)
             // (mod 3) of the CTA's last tile, staged in the operand ring, which
-            // no MMA reads any more once that tile's accumulator is complete.
+            // no MMA reads any more once that tile's accumulator is complete
+            // (signalled on tlast, which only the last tile's commit reaches).
             const int hq = warp & 3, hslot = 1 + ((warp - 6) >> 2);
             const uint32_t hacc = (uint32_t)((my_tiles - 1) & 1);
-            const uint32_t hphase = (uint32_t)(((my_tiles - 1) >> 1) & 1);
             int n, toh, tow, cb;
             vconv_tile(t_last, p, n, toh, tow, cb);
             const int co_row0 = cb * 128 + hq * 32;
             const int co = co_row0 + lane;
             const float brow = (p.bias != nullptr && co < p.Co) ? __ldg(p.bias + co) : 0.0f;
-            if (warp_epi_wait(pp, pp.tfull0 + 8 * hacc, hphase)) {
+            if (warp_epi_wait(pp, tlast, 0)) {
                 ptx::tc_fence_after();
                 const uint32_t tbase = pp.tmem + ((uint32_t)(hq * 32) << 16) + hacc * BN;
                 const uint32_t hbuf = sB + (uint32_t)(warp - 6) * 8192u;
@@ -498,16 +500,16 @@ __global__ void __launch_bounds__(ConvVecCfg<WIN>::THREADS, 1)
             // ------------------------------- help with the last tile's epilogue --
             // Gather warp g (lane quarter g & 3) takes units u = 1 + (g >> 2)
             // (mod 3) of the CTA's last tile, staged in the operand ring, which
-            // no MMA reads any more once that tile's accumulator is complete.
+            // no MMA reads any more once that tile's accumulator is complete
+            // (signalled on tlast, which only the last tile's commit reaches).
             const int hq = warp & 3, hslot = 1 + ((warp - 6) >> 2);
             const uint32_t hacc = (uint32_t)((my_tiles - 1) & 1);
-            const uint32_t hphase = (uint32_t)(((my_tiles - 1) >> 1) & 1);
             int n, toh, tow, cb;
             vconv_tile(t_last, p, n, toh, tow, cb);
             const int co_row0 = cb * 128 + hq * 32;
             const int co = co_row0 + lane;
             const float brow = (p.bias != nullptr && co < p.Co) ? __ldg(p.bias + co) : 0.0f;
-            if (warp_epi_wait(pp, pp.tfull0 + 8 * hacc, hphase)) {
+            if (warp_epi_wait(pp, tlast, 0)) {
                 ptx::tc_fence_after();
                 const uint32_t tbase = pp.tmem + ((uint32_t)(hq * 32) << 16) + hacc * BN;
                 const uint32_t hbuf = sB + (uint32_t)(warp - 6) * 8192u;

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "mmact.h"
+
 namespace mmact {
 
 struct GemmArgs {
@@ -106,6 +108,50 @@ struct NhwcLaunch {
     int grid;
 };
 
+// NCHW conv with the im2col operand in tensor memory (conv_tmem.cu).
+// Largest raw input window (bytes) staged per K block, and the size of the
+// K-offset table (entries: lcm(64, kh*kw) must fit).
+constexpr int CONV_TMEM_WIN_MAX_BYTES = 40960;
+constexpr int CONV_TMEM_TABLE_MAX = 3136;
+constexpr int CONV_TMEM_MAX_WSTAGES = 8;
+
+struct TmemConvArgs {
+    int Nb, C, H, W, Co, kh, kw;
+    int sh, sw, pt, pl, dh, dw;
+    int Ho, Wo, P, K;
+    int tiles_co, tiles_p, num_tiles, num_kb;   // tiles: 128 consecutive pixels of one image x BN channels
+    int ab_bf16;
+    int act;
+    float alpha;
+    int WB, HB, CB;      // raw window per K block: WB columns x HB rows x CB channels
+    int esh;             // TMA row traversal stride of the window (sh when every used row is a multiple of sh apart)
+    int rowmul, rstep;   // window rows per output row of the tile, per filter row r
+    int x0, xoff;        // window column origin (8-aligned) and -pl - x0
+    int raw_bytes;
+    int win_slot;        // bytes per window slot (raw_bytes rounded up to 1 KB)
+    int wstages;         // window slots in the ring (2..CONV_TMEM_MAX_WSTAGES)
+    int y_tma;           // 1: output blocks by TMA store (P * out bytes a multiple of 16)
+    int tab_period;      // K-offset table covers tab_period blocks of 64 (the pattern's period)
+    const float *bias;
+    const void *res;     // residual shaped like y (output dtype), or null
+    void *y;
+    unsigned int *status;
+    unsigned long long wait_ns;
+};
+
+struct TmemConvLaunch {
+    CUtensorMap tmW, tmX, tmY;   // filter as {K, Co}; x as {W, H, C, N}; y as {P, Co, N}
+    TmemConvArgs args;
+    int tile_n;             // BN: 64, 128 or 256 output channels per tile
+    int out;
+    int grid;
+};
+
+cudaError_t setup_conv_tmem_kernels();
+cudaError_t launch_conv_tmem(const TmemConvLaunch &L, cudaStream_t stream);
+// Bytes of shared memory the kernel with tile_n output channels leaves for its window ring.
+int conv_tmem_window_region(int tile_n);
+
 cudaError_t setup_nhwc_kernels();
 cudaError_t launch_conv_nhwc(const NhwcLaunch &L, cudaStream_t stream);
 cudaError_t launch_gemm(const GemmLaunch &L, cudaStream_t stream);
@@ -133,5 +179,10 @@ cudaError_t launch_bias_act(const float *bias, void *out, int64_t rows, int64_t 
                             cudaStream_t stream, const void *res = nullptr);
 cudaError_t launch_wait_selftest(unsigned int *status, unsigned long long timeout_ns,
                                  cudaStream_t stream);
+
+// Host argument checks of the mmact_gemm family (api.cu): MMACT_OK (0), or the
+// status the entry points return for these arguments.
+mmact_status gemm_check(const void *A, const void *B, const float *bias, const void *C, int64_t M,
+                        int64_t N, int64_t K, mmact_dtype ab, mmact_dtype cd, mmact_act act);
 
 }  // namespace mmact

@@ -16,12 +16,17 @@
 // process exits.  Host code cannot use the symbol itself as a device
 // address (on the host it names a shadow variable), so the first call on each
 // device asks the runtime for the array's device address with
-// cudaGetSymbolAddress, with that device current, and caches it.
+// cudaGetSymbolAddress, with that device current, and caches it.  The cache
+// entry is tied to the CUDA context it was looked up in (by the context's
+// process-unique id): after cudaDeviceReset the next call finds a new context
+// and looks the address up again instead of reusing a stale one.
 #include <cstdint>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "kernels.h"
 #include "mmact.h"
 
 #define MMACT_EXPORT extern "C" __attribute__((visibility("default")))
@@ -31,22 +36,59 @@ namespace {
 static __device__ __align__(256) float g_noalloc_scratch[MMACT_NOALLOC_MAX_ELEMENTS];
 
 constexpr int MAX_DEVICES = 64;
-float *g_scratch_ptr[MAX_DEVICES] = {};
+struct ScratchEntry {
+    unsigned long long ctx_id = 0;   // id of the context the address belongs to (0: none yet)
+    float *ptr = nullptr;
+};
+ScratchEntry g_scratch[MAX_DEVICES];
 std::mutex g_scratch_mutex;
 
-// Device address of this device's scratch array (looked up once per device).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+template <typename Fn>
+bool driver_entry(const char *name, Fn *out)
+{
+    if (*out != nullptr) return true;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+    *out = reinterpret_cast<Fn>(fn);
+    return true;
+}
+
+// Device address of the current device's scratch array in the current
+// context: looked up once per device and context, under a lock.
 mmact_status scratch_address(float **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return MMACT_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    if (!driver_entry("cuCtxGetCurrent", &g_ctx_get_current) || !driver_entry("cuCtxGetId", &g_ctx_get_id))
+        return MMACT_ERR_CUDA;
+    // id of the current context, 0 when the runtime has not made one current yet
+    auto current_id = [](unsigned long long *id) {
+        CUcontext ctx = nullptr;
+        *id = 0;
+        if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return false;
+        return ctx == nullptr || g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+    };
+    unsigned long long id = 0;
+    if (!current_id(&id)) return MMACT_ERR_CUDA;
+    ScratchEntry &e = g_scratch[dev];
+    if (id == 0 || e.ptr == nullptr || e.ctx_id != id) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
             return MMACT_ERR_CUDA;
-        g_scratch_ptr[dev] = static_cast<float *>(p);
+        if (!current_id(&id) || id == 0) return MMACT_ERR_CUDA;   // the lookup made the context current
+        e.ptr = static_cast<float *>(p);
+        e.ctx_id = id;
     }
-    *out = g_scratch_ptr[dev];
+    *out = e.ptr;
     return MMACT_OK;
 }
 
@@ -57,11 +99,13 @@ MMACT_EXPORT mmact_status mmact_gemm_split_noalloc(const void *A, const void *B,
                                                    mmact_dtype ab_dtype, mmact_dtype c_dtype,
                                                    mmact_act act, float alpha, void *stream)
 {
-    const int64_t max_dim = (int64_t(1) << 31) - 1;
-    if (M < 0 || N < 0 || M > max_dim || N > max_dim) return MMACT_ERR_INVALID_ARG;
+    // the same argument checks as mmact_gemm_split, before anything else
+    mmact_status s = mmact::gemm_check(A, B, bias, C, M, N, K, ab_dtype, c_dtype, act);
+    if (s != MMACT_OK) return s;
     if (M * N > (int64_t)MMACT_NOALLOC_MAX_ELEMENTS) return MMACT_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return MMACT_OK;
     float *ws = nullptr;
-    const mmact_status s = scratch_address(&ws);
+    s = scratch_address(&ws);
     if (s != MMACT_OK) return s;
     // The first kernel overwrites all M*N workspace elements before the
     // second reads them, so nothing left by an earlier call is ever read.

@@ -31,7 +31,8 @@ SYMBOLS = [
     "mmact_conv2d_out_shape", "mmact_conv2d_producer", "mmact_get_last_error",
     "mmact_set_wait_timeout_ns",
     "mmact_selftest_wait_timeout", "mmact_set_gemm_tile_n", "mmact_set_gemm_split_k",
-    "mmact_gemm_split_k_choice", "mmact_set_gemm_pair", "mmact_gemm_kernel_choice", "mmact_status_string", "mmact_version",
+    "mmact_gemm_split_k_choice", "mmact_set_gemm_pair", "mmact_gemm_kernel_choice", "mmact_set_conv_tmem",
+    "mmact_status_string", "mmact_version",
 ]
 
 
@@ -81,6 +82,7 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     L.mmact_set_gemm_tile_n.argtypes = [ci]
     L.mmact_set_gemm_split_k.argtypes = [ci]
     L.mmact_set_gemm_pair.argtypes = [ci]
+    L.mmact_set_conv_tmem.argtypes = [ci]
     L.mmact_gemm_kernel_choice.argtypes = [i64, i64, i64, ci, ctypes.POINTER(ci)]
     L.mmact_gemm_split_k_choice.argtypes = [i64, i64, i64, ctypes.POINTER(ci)]
     L.mmact_status_string.argtypes = [ci]
@@ -89,7 +91,8 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     for name in ("mmact_gemm", "mmact_gemm_split", "mmact_conv2d", "mmact_conv2d_split",
                  "mmact_conv2d_out_shape", "mmact_get_last_error", "mmact_selftest_wait_timeout",
                  "mmact_set_gemm_tile_n", "mmact_set_gemm_split_k", "mmact_gemm_split_k_choice",
-                 "mmact_set_gemm_pair", "mmact_gemm_kernel_choice", "mmact_version"):
+                 "mmact_set_gemm_pair", "mmact_gemm_kernel_choice", "mmact_set_conv_tmem",
+                 "mmact_version"):
         getattr(L, name).restype = ci
     _lib = L
     return L
@@ -210,7 +213,7 @@ def mmact_conv2d_out_shape(H, W, kh, kw, stride, pads, dilation) -> tuple:
     return ho.value, wo.value
 
 
-CONV_PRODUCER = {0: "gather", 1: "vector", 2: "window"}
+CONV_PRODUCER = {0: "gather", 1: "vector", 2: "window", 3: "tmem"}
 
 
 def mmact_conv2d_producer(N, C, H, W, Co, kh, kw, stride, pads, dilation, in_dtype, out_dtype) -> str:
@@ -342,6 +345,11 @@ def mmact_set_gemm_split_k(split_k: int) -> None:
 def mmact_set_gemm_pair(mode: int) -> None:
     """CTA-pair GEMM kernel: 0 chosen per shape; 1 never; 2 always (when split-K is not taken)."""
     _check(load().mmact_set_gemm_pair(int(mode)), "mmact_set_gemm_pair")
+
+
+def mmact_set_conv_tmem(mode: int) -> None:
+    """NCHW conv with the im2col operand in tensor memory: 0 where it applies (default); 1 never."""
+    _check(load().mmact_set_conv_tmem(int(mode)), "mmact_set_conv_tmem")
 
 
 GEMM_KERNELS = {0: "none", 1: "persistent", 2: "pair", 3: "split_k"}

@@ -202,15 +202,21 @@ mmact_status mmact_conv2d_split(const void *x, const void *w, const float *bias,
  *     (nothing enqueued).  Every GPU that loads the library holds the 16 MiB
  *     array until the process exits.
  *   - Set-up: the first call on each device looks up the array's device
- *     address (cudaGetSymbolAddress, with that device current) and caches it;
- *     make that first call before any stream capture.
+ *     address (cudaGetSymbolAddress, with that device current) and caches it
+ *     for that device's current CUDA context; make that first call before any
+ *     stream capture.  A call in a new context (after cudaDeviceReset) looks
+ *     the address up again, so the same rule applies to it.
  *   - Sharing: all calls on a device share the one array, which keeps the
  *     last call's intermediate values.  Nothing in it needs clearing: the
  *     first kernel overwrites every element it uses before the second reads
  *     it.  Calls whose kernels may overlap on the GPU (different streams, or
  *     several host threads without ordering) race on the array; order them,
  *     e.g. on one stream.
- * All other behaviour, layouts and errors are those of mmact_gemm_split.
+ * Argument checks are those of mmact_gemm_split and come first (a bad
+ * pointer, dtype or activation returns MMACT_ERR_INVALID_ARG whatever the
+ * size); the size limit is checked next, and the scratch address is looked
+ * up only for a call that will run.  All other behaviour, layouts and errors
+ * are those of mmact_gemm_split.
  */
 mmact_status mmact_gemm_split_noalloc(const void *A, const void *B, const float *bias, void *C,
                                       int64_t M, int64_t N, int64_t K,
@@ -277,8 +283,20 @@ mmact_status mmact_conv2d_out_shape(int64_t H, int64_t W, int64_t kh, int64_t kw
  *   MMACT_CONV_WINDOW  as VECTOR, but each K block's input window is first
  *                      loaded into shared memory by one TMA box (when that
  *                      window fits in 24 KB)
+ *   MMACT_CONV_TMEM    the im2col operand is assembled in tensor memory, one
+ *                      output pixel per TMEM lane, from each K block's input
+ *                      window (staged by TMA); the filter is the MMA's
+ *                      shared-memory operand (16-bit inputs, W % 8 == 0,
+ *                      C*kh*kw % 8 == 0, a window of at most 40 KB, and
+ *                      lcm(64, kh*kw) <= 3136).  Taken whenever it applies,
+ *                      unless mmact_set_conv_tmem(1) turned it off.
  */
-typedef enum { MMACT_CONV_GATHER = 0, MMACT_CONV_VECTOR = 1, MMACT_CONV_WINDOW = 2 } mmact_conv_producer;
+typedef enum {
+    MMACT_CONV_GATHER = 0,
+    MMACT_CONV_VECTOR = 1,
+    MMACT_CONV_WINDOW = 2,
+    MMACT_CONV_TMEM = 3
+} mmact_conv_producer;
 int mmact_conv2d_producer(int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh,
                           int64_t kw, const int32_t strides[2], const int32_t pads[4],
                           const int32_t dilations[2], mmact_dtype in_dtype, mmact_dtype out_dtype);
@@ -339,6 +357,16 @@ mmact_status mmact_set_gemm_split_k(int split_k);
  * process.  Returns MMACT_ERR_INVALID_ARG for other values.
  */
 mmact_status mmact_set_gemm_pair(int mode);
+
+/*
+ * Tuning and testing aid (no counterpart in the pages: a GB300 execution
+ * choice for the same operator): whether mmact_conv2d, mmact_conv2d_residual
+ * and mmact_conv2d_split use the tensor-memory im2col kernel
+ * (MMACT_CONV_TMEM) where it applies.  mode: 0 = yes (the default), 1 = never
+ * (the window / vector / gather producers).  Applies to later calls in the
+ * process.  Returns MMACT_ERR_INVALID_ARG for other values.
+ */
+mmact_status mmact_set_conv_tmem(int mode);
 
 /* The GEMM kernels an mmact_gemm-family call can run. */
 typedef enum {

@@ -90,19 +90,39 @@ def test_conv_producer_choice(lib):
     import torch
     f16, bf16, f32 = torch.float16, torch.bfloat16, torch.float32
     P = mmact.mmact_conv2d_producer
-    # the three conv workloads
-    assert P(8, 64, 56, 56, 128, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1), f16, f16) == "window"
-    assert P(16, 128, 64, 64, 256, 3, 3, (2, 2), (2, 2, 2, 2), (2, 2), bf16, bf16) == "window"
-    # 1x1, 64 channels per K block: the window would be 72 x 8 x 64 x 2 B > 24 KB
-    assert P(16, 128, 64, 64, 256, 1, 1, (2, 2), (0, 0, 0, 0), (1, 1), bf16, bf16) == "vector"
-    # input width not a multiple of 8, horizontal stride 3, K not a multiple of 8
-    assert P(2, 24, 17, 13, 40, 3, 3, (2, 2), (2, 2, 2, 2), (2, 2), bf16, bf16) == "gather"
-    assert P(1, 8, 16, 48, 8, 3, 3, (1, 3), (1, 1, 1, 1), (1, 1), f16, f16) == "gather"
-    assert P(3, 3, 11, 16, 5, 3, 2, (2, 1), (1, 0, 2, 1), (1, 2), f16, f32) == "gather"
-    # dh not a multiple of sh: the window keeps every input row
-    assert P(1, 16, 7, 16, 16, 3, 3, (2, 1), (1, 1, 2, 2), (1, 2), bf16, f16) == "window"
+    try:
+        # default: the tensor-memory im2col kernel wherever it applies -- the three conv workloads
+        assert P(8, 64, 56, 56, 128, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1), f16, f16) == "tmem"
+        assert P(16, 128, 64, 64, 256, 3, 3, (2, 2), (2, 2, 2, 2), (2, 2), bf16, bf16) == "tmem"
+        assert P(16, 128, 64, 64, 256, 1, 1, (2, 2), (0, 0, 0, 0), (1, 1), bf16, bf16) == "tmem"
+        assert P(1, 16, 7, 16, 16, 3, 3, (2, 1), (1, 1, 2, 2), (1, 2), bf16, f16) == "tmem"
+        # it does not apply: input width not a multiple of 8, K not a multiple of 8, 11x11 taps
+        assert P(2, 24, 17, 13, 40, 3, 3, (2, 2), (2, 2, 2, 2), (2, 2), bf16, bf16) == "gather"
+        assert P(3, 3, 11, 16, 5, 3, 2, (2, 1), (1, 0, 2, 1), (1, 2), f16, f32) == "gather"
+        assert P(1, 8, 64, 64, 8, 11, 11, (1, 1), (5, 5, 5, 5), (1, 1), f16, f16) == "window"
+        # with it turned off: the window / vector / gather producers
+        mmact.mmact_set_conv_tmem(1)
+        assert P(8, 64, 56, 56, 128, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1), f16, f16) == "window"
+        assert P(16, 128, 64, 64, 256, 3, 3, (2, 2), (2, 2, 2, 2), (2, 2), bf16, bf16) == "window"
+        # 1x1, 64 channels per K block: the window would be 72 x 8 x 64 x 2 B > 24 KB
+        assert P(16, 128, 64, 64, 256, 1, 1, (2, 2), (0, 0, 0, 0), (1, 1), bf16, bf16) == "vector"
+        # input width not a multiple of 8, horizontal stride 3, K not a multiple of 8
+        assert P(2, 24, 17, 13, 40, 3, 3, (2, 2), (2, 2, 2, 2), (2, 2), bf16, bf16) == "gather"
+        assert P(1, 8, 16, 48, 8, 3, 3, (1, 3), (1, 1, 1, 1), (1, 1), f16, f16) == "gather"
+        assert P(3, 3, 11, 16, 5, 3, 2, (2, 1), (1, 0, 2, 1), (1, 2), f16, f32) == "gather"
+        # dh not a multiple of sh: the window keeps every input row
+        assert P(1, 16, 7, 16, 16, 3, 3, (2, 1), (1, 1, 2, 2), (1, 2), bf16, f16) == "window"
+    finally:
+        mmact.mmact_set_conv_tmem(0)
     with pytest.raises(ValueError):
         P(1, 8, 8, 8, 8, 0, 3, (1, 1), (0, 0, 0, 0), (1, 1), f16, f16)
+
+
+def test_conv_tmem_mode_validation(lib):
+    for bad in (-1, 2, 3):
+        assert lib.mmact_set_conv_tmem(bad) == mmact.MMACT_ERR_INVALID_ARG
+    for good in (1, 0):
+        assert lib.mmact_set_conv_tmem(good) == mmact.MMACT_OK
 
 
 def test_out_shape_rejects_bad_geometry(lib):
@@ -153,6 +173,25 @@ def test_gemm_host_validation(lib):
     assert gemm(lib, split=True, ws=None) == E
     assert gemm(lib, split=True, ws=P_MIS) == U
     assert gemm(lib, split=True, ws=P16, M=0) == OK
+
+
+def test_noalloc_checks_arguments_before_its_size_limit(lib):
+    # the same checks as mmact_gemm_split come first: a bad argument is reported
+    # as such even when M*N is beyond the scratch array; then the size limit
+    E, U, OK = mmact.MMACT_ERR_INVALID_ARG, mmact.MMACT_ERR_UNSUPPORTED, mmact.MMACT_OK
+    big_m, big_n = 4096, 4096                  # 4 x MMACT_NOALLOC_MAX_ELEMENTS
+
+    def na(A=P16, C=P16, M=64, N=64, K=64, ab=1, cd=1, act=2):
+        return lib.mmact_gemm_split_noalloc(A, P16, None, C, M, N, K, ab, cd, act, ctypes.c_float(0.1), None)
+
+    assert na(act=9, M=big_m, N=big_n) == E
+    assert na(ab=2, M=big_m, N=big_n) == E
+    assert na(A=None, M=big_m, N=big_n) == E
+    assert na(M=-1) == E
+    assert na(A=P_MIS, M=big_m, N=big_n) == U   # alignment, as for mmact_gemm_split
+    assert na(M=big_m, N=big_n) == U            # valid arguments, beyond the scratch array
+    assert na(M=2048, N=2056) == U              # just past the limit (2048 x 2048 is the largest square)
+    assert na(M=0) == OK                        # empty: nothing enqueued, no set-up
 
 
 def test_gemm_residual_host_validation(lib):

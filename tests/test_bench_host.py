@@ -34,8 +34,42 @@ def test_conv_flops_and_bytes(lib):
     Ho, Wo = mmact.mmact_conv2d_out_shape(wl.H, wl.W, wl.kh, wl.kw, wl.stride, wl.pads, wl.dilation)
     assert (Ho, Wo) == (32, 32)     # (64 + 2 + 2 - 2 * 2 - 1) // 2 + 1
     assert bench.workload_flops(mmact, wl) == 2.0 * 16 * 32 * 32 * 256 * 128 * 9
-    assert bench.workload_bytes(mmact, wl) == (2.0 * (16 * 128 * 64 * 64 + 256 * 128 * 9) + 4.0 * 256
+    # stride 2, dilation 2, pad 2: outputs read only the even input rows and columns (32 of 64 each)
+    assert bench.workload_bytes(mmact, wl) == (2.0 * (16 * 128 * 32 * 32 + 256 * 128 * 9) + 4.0 * 256
                                               + 2.0 * 16 * 256 * 32 * 32)
+
+
+def test_conv_input_lines_read():
+    # 3x3, stride 1, pad 1 on 56: every line; 1x1 stride 2 on 64: the 32 even lines;
+    # 3x3 stride 2 dilation 2 pad 2 on 64: the even lines; 3x3 stride 2 pad 1: every line
+    assert bench.conv_lines_read(56, 3, 1, 1, 1, 56) == 56
+    assert bench.conv_lines_read(64, 1, 2, 0, 1, 32) == 32
+    assert bench.conv_lines_read(64, 3, 2, 2, 2, 32) == 32
+    assert bench.conv_lines_read(64, 3, 2, 1, 1, 32) == 64
+    # a 1x1 stride-2 conv needs a quarter of x
+    wl = synth.WORKLOADS["conv1x1_s2_tanh_16x128x64x64_bf16"]
+    x_needed = 2.0 * 16 * 128 * 32 * 32
+    assert bench.workload_bytes(lib_free_shape(wl), wl) == (x_needed + 2.0 * 256 * 128 + 4.0 * 256
+                                                            + 2.0 * 16 * 256 * 32 * 32)
+
+
+def lib_free_shape(wl):
+    """Stand-in for the library's output-shape call (the formula, for these tests only)."""
+    class Shape:
+        @staticmethod
+        def mmact_conv2d_out_shape(H, W, kh, kw, st, pd, dl):
+            return ((H + pd[0] + pd[1] - dl[0] * (kh - 1) - 1) // st[0] + 1,
+                    (W + pd[2] + pd[3] - dl[1] * (kw - 1) - 1) // st[1] + 1)
+    return Shape
+
+
+def test_tensor_capacity_fractions():
+    rec = bench.tensor_capacity(1872.0, 152, 1537.0, 2070.0)
+    cap = 152 * 8192 * 1537e6 / 1e12
+    assert rec["peak_tflops_at_sampled_clock"] == pytest.approx(cap)
+    assert rec["frac_at_sampled_clock"] == pytest.approx(1872.0 / cap)
+    assert rec["peak_tflops_at_max_clock"] == pytest.approx(152 * 8192 * 2070e6 / 1e12)
+    assert rec["frac_of_nominal"] == pytest.approx(1872.0 / 2250.0)
 
 
 def test_roofline_bound_follows_the_ridge_point():

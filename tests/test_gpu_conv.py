@@ -3,8 +3,9 @@
 Small geometries sweep stride, padding (asymmetric too), dilation, kernel
 size, channel counts that leave ragged K / Co / pixel tiles, and the
 fallback paths (filter rows whose pitch rules out TMA, outputs whose pitch
-rules out TMA stores).  The full workloads are compared in full or on seeded
-samples of output elements.
+rules out TMA stores), each under both NCHW kernel families (the tensor-memory
+im2col kernel where it applies, and the window / vector / gather producers).
+The full workloads are compared element by element.
 """
 import numpy as np
 import pytest
@@ -12,7 +13,7 @@ import torch
 
 import oracle
 from conv_activation_epilogue_gb300 import build, mmact, synth
-from parity import TORCH, check, fp32_to_device, host, sample_points, to_device
+from parity import TORCH, check, fp32_to_device, host, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -26,6 +27,22 @@ def lib():
 @pytest.fixture(scope="module")
 def orc():
     return oracle.get()
+
+
+@pytest.fixture(params=["tmem", "legacy"])
+def conv_mode(request):
+    """NCHW kernel family: the tensor-memory im2col kernel where it applies, or
+    the window / vector / gather producers everywhere."""
+    mmact.mmact_set_conv_tmem(0 if request.param == "tmem" else 1)
+    yield request.param
+    mmact.mmact_set_conv_tmem(0)
+
+
+@pytest.fixture
+def legacy_mode():
+    mmact.mmact_set_conv_tmem(1)
+    yield
+    mmact.mmact_set_conv_tmem(0)
 
 
 def run_conv(x, w, bias, dt, od, stride, pads, dil, act, alpha=0.0, split=False):
@@ -54,6 +71,7 @@ CASES = [
     (2, 72, 9, 15, 8, 5, 5, (1, 2), (2, 2, 1, 3), (1, 1), "bf16", "bf16"),   # K not a multiple of 64
     (1, 16, 30, 30, 64, 7, 7, (2, 2), (3, 3, 3, 3), (1, 1), "f16", "f16"),
     (1, 4, 5, 5, 3, 5, 5, (1, 1), (0, 0, 0, 0), (1, 1), "f16", "bf16"),      # one output pixel
+    (16, 16, 64, 64, 128, 1, 1, (1, 1), (0, 0, 0, 0), (1, 1), "f16", "f16"), # one K block, several tiles a CTA
 ]
 
 
@@ -79,7 +97,7 @@ VEC_PRODUCERS = ["window", "window", "window", "vector", "window", "window", "wi
                  "window", "window"]
 
 
-def test_vectorised_cases_cover_both_producers():
+def test_vectorised_cases_cover_both_producers(legacy_mode):
     for case, want in zip(VEC_CASES, VEC_PRODUCERS, strict=True):
         Nb, C, H, W, Co, kh, kw, st, pd, dl, dt, od = case
         assert mmact.mmact_conv2d_producer(Nb, C, H, W, Co, kh, kw, st, pd, dl, TORCH[dt], TORCH[od]) == want, case
@@ -91,13 +109,13 @@ def test_vectorised_cases_cover_both_producers():
 
 @pytest.mark.parametrize("case", VEC_CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}x{c[3]}-{c[4]}k{c[5]}{c[6]}s{c[7][0]}{c[7][1]}")
 @pytest.mark.parametrize("act", ["tanh", "relu", "sigmoid", "gelu"])
-def test_vectorised_geometries(orc, case, act):
-    test_small_geometries(orc, case, act)
+def test_vectorised_geometries(orc, case, act, conv_mode):
+    test_small_geometries(orc, case, act, conv_mode)
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}x{c[3]}-{c[4]}k{c[5]}{c[6]}s{c[7][0]}{c[7][1]}")
 @pytest.mark.parametrize("act", ["tanh", "leaky_relu", "sigmoid", "gelu"])
-def test_small_geometries(orc, case, act):
+def test_small_geometries(orc, case, act, conv_mode):
     Nb, C, H, W, Co, kh, kw, stride, pads, dil, dt, od = case
     rng = np.random.default_rng(Nb * 1000 + C * 10 + Co)
     x = synth.to_codes(rng.normal(0, 1, (Nb, C, H, W)), dt)
@@ -131,18 +149,25 @@ def test_zero_input_channels_gives_act_of_bias(orc):
 CONV_WORKLOADS = [w for w in synth.WORKLOADS.values() if w.kind == "conv"]
 
 
+_FULL_REF = {}
+
+
+def workload_reference(orc, wl, inp):
+    """Every output element of a conv workload from the oracle (computed once per run)."""
+    if wl.name not in _FULL_REF:
+        _FULL_REF[wl.name] = orc.conv2d(inp["x"], inp["w"], wl.dtype, inp["bias"], wl.stride, wl.pads,
+                                        wl.dilation, wl.act, wl.alpha).ravel()
+    return _FULL_REF[wl.name]
+
+
 @pytest.mark.parametrize("wl", CONV_WORKLOADS, ids=lambda w: w.name)
 @pytest.mark.parametrize("split", [False, True], ids=["fused", "split"])
-def test_workload_parity(orc, wl, split):
+def test_workload_parity(orc, wl, split, conv_mode):
+    # every output element of the workload against the oracle (1.8e9-4.8e9 fp64 MACs each)
     inp = wl.inputs()
+    if conv_mode == "tmem":
+        assert mmact.mmact_conv2d_producer(wl.N, wl.C, wl.H, wl.W, wl.Co, wl.kh, wl.kw, wl.stride, wl.pads,
+                                           wl.dilation, TORCH[wl.dtype], TORCH[wl.out_dtype]) == "tmem"
     y = run_conv(inp["x"], inp["w"], inp["bias"], wl.dtype, wl.out_dtype, wl.stride, wl.pads,
                  wl.dilation, wl.act, wl.alpha, split=split)
-    got = host(y).ravel()
-    n_out = got.size
-    pts = sample_points(n_out, y.shape[0] * y.shape[1], y.shape[2] * y.shape[3], 20000, wl.seed)
-    # plus one whole output plane (image 0, channel 0) and the last one
-    plane = y.shape[2] * y.shape[3]
-    pts = np.unique(np.concatenate([pts, np.arange(plane), np.arange(n_out - plane, n_out)]))
-    ref = orc.conv2d(inp["x"], inp["w"], wl.dtype, inp["bias"], wl.stride, wl.pads, wl.dilation,
-                     wl.act, wl.alpha, points=pts)
-    check(got[pts], ref, wl.out_dtype, wl.name)
+    check(host(y).ravel(), workload_reference(orc, wl, inp), wl.out_dtype, wl.name)

@@ -82,10 +82,10 @@ def test_workload_shapes_channels_last(orc, wl):
     inp = wl.inputs()
     y = run_nhwc(inp["x"], inp["w"], inp["bias"], wl.dtype, wl.out_dtype, wl.stride, wl.pads,
                  wl.dilation, wl.act, wl.alpha).ravel()
-    pts = sample_points(y.size, y.size // 64, 64, 20000, wl.seed + 100)
+    # every output element against the oracle
     ref = orc.conv2d(inp["x"], inp["w"], wl.dtype, inp["bias"], wl.stride, wl.pads, wl.dilation,
-                     wl.act, wl.alpha, points=pts)
-    check(y[pts], ref, wl.out_dtype, f"nhwc {wl.name}")
+                     wl.act, wl.alpha).ravel()
+    check(y, ref, wl.out_dtype, f"nhwc {wl.name}")
 
 
 # ---------------------------------------------------------------- fp32 inputs --

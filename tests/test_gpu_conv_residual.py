@@ -45,11 +45,22 @@ NCHW_CASES = [
 ]
 
 
+@pytest.fixture(params=["tmem", "legacy"])
+def conv_mode(request):
+    mmact.mmact_set_conv_tmem(0 if request.param == "tmem" else 1)
+    yield request.param
+    mmact.mmact_set_conv_tmem(0)
+
+
 @pytest.mark.parametrize("case", NCHW_CASES, ids=lambda c: f"{c[-1]}-{c[0]}x{c[1]}x{c[2]}x{c[3]}-{c[4]}k{c[5]}{c[6]}")
 @pytest.mark.parametrize("act", ["tanh", "relu"])
-def test_nchw_residual(orc, case, act):
+def test_nchw_residual(orc, case, act, conv_mode):
     Nb, C, H, W, Co, kh, kw, st, pd, dl, dt, od, producer = case
-    assert mmact.mmact_conv2d_producer(Nb, C, H, W, Co, kh, kw, st, pd, dl, TORCH[dt], TORCH[od]) == producer
+    got_producer = mmact.mmact_conv2d_producer(Nb, C, H, W, Co, kh, kw, st, pd, dl, TORCH[dt], TORCH[od])
+    if conv_mode == "legacy":
+        assert got_producer == producer
+    else:
+        assert got_producer == ("tmem" if producer in ("window", "vector") else producer)
     rng = np.random.default_rng(Nb * 7 + C + Co)
     x = synth.to_codes(rng.normal(0, 1, (Nb, C, H, W)), dt)
     w = synth.to_codes(rng.normal(0, (1.0 / (C * kh * kw)) ** 0.5, (Co, C, kh, kw)), dt)
@@ -64,7 +75,7 @@ def test_nchw_residual(orc, case, act):
     check(host(y), ref, od, f"nchw residual {case} {act}")
 
 
-def test_nchw_residual_in_place(orc):
+def test_nchw_residual_in_place(orc, conv_mode):
     rng = np.random.default_rng(41)
     Nb, C, H, W, Co = 2, 32, 20, 40, 64
     x = synth.to_codes(rng.normal(0, 1, (Nb, C, H, W)), "bf16")

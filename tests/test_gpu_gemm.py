@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from conv_activation_epilogue_gb300 import build, mmact, synth
-from parity import TORCH, check, fp32_to_device, host, sample_points, to_device
+from parity import TORCH, check, fp32_to_device, host, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -146,6 +146,24 @@ def test_identity_B_returns_act_of_A_plus_bias(orc):
 GEMM_WORKLOADS = [w for w in synth.WORKLOADS.values() if w.kind == "gemm"]
 
 
+_REF = {}
+
+
+def workload_points(wl):
+    """Output elements compared for a GEMM workload: all of them, except for the 8192^3 one
+    (5.5e11 fp64 MACs), where every element of 512 seeded random rows and of 512 seeded
+    random columns is compared (8.4 million elements)."""
+    M, N = wl.M, wl.N
+    if M * N * wl.K <= 2 ** 37:
+        return None
+    rng = np.random.default_rng(wl.seed)
+    rows = rng.choice(M, 512, replace=False)
+    cols = rng.choice(N, 512, replace=False)
+    pts = np.concatenate([(rows[:, None] * N + np.arange(N)[None, :]).ravel(),
+                          (np.arange(M)[:, None] * N + cols[None, :]).ravel()])
+    return np.unique(pts.astype(np.int64))
+
+
 @pytest.mark.parametrize("wl", GEMM_WORKLOADS, ids=lambda w: w.name)
 @pytest.mark.parametrize("split", [False, True], ids=["fused", "split"])
 def test_workload_parity(orc, wl, split):
@@ -153,11 +171,8 @@ def test_workload_parity(orc, wl, split):
     C, _ = run_gemm(inp["A"], inp["B"], inp["bias"], wl.ab_dtype, wl.c_dtype, wl.act, wl.alpha,
                     split=split)
     got = host(C).ravel()
-    M, N = wl.M, wl.N
-    if M * N * wl.K <= 2 ** 28:      # small enough to compare every element
-        ref = orc.gemm(inp["A"], inp["B"], wl.ab_dtype, inp["bias"], wl.act, wl.alpha).ravel()
-        check(got, ref, wl.c_dtype, wl.name)
-    else:
-        pts = sample_points(M * N, M, N, 6000, seed=wl.seed)
-        ref = orc.gemm(inp["A"], inp["B"], wl.ab_dtype, inp["bias"], wl.act, wl.alpha, points=pts)
-        check(got[pts], ref, wl.c_dtype, wl.name)
+    pts = workload_points(wl)
+    if wl.name not in _REF:       # the oracle's values, shared by the fused and split runs
+        _REF[wl.name] = orc.gemm(inp["A"], inp["B"], wl.ab_dtype, inp["bias"], wl.act, wl.alpha,
+                                 points=pts).ravel()
+    check(got if pts is None else got[pts], _REF[wl.name], wl.c_dtype, wl.name)

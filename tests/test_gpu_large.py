@@ -49,7 +49,7 @@ def test_gemm_output_beyond_2_31_elements(orc):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("layout", ["nchw", "nhwc"])
+@pytest.mark.parametrize("layout", ["nchw", "nchw_window", "nhwc"])
 def test_conv_output_beyond_2_31_elements(orc, layout):
     Nb, C, H, W, Co = 8192, 64, 56, 56, 128
     rng = np.random.default_rng(62)
@@ -62,13 +62,18 @@ def test_conv_output_beyond_2_31_elements(orc, layout):
     total = Nb * Co * H * W
     pts = np.concatenate([rng.integers(0, total, 3000, dtype=np.int64),
                           np.array([total - 1, 2 ** 31, 2 ** 31 - 1, 3 * 2 ** 30], dtype=np.int64)])
-    if layout == "nchw":
-        assert mmact.mmact_conv2d_producer(Nb, C, H, W, Co, 3, 3, st, pd, dl, torch.float16,
-                                           torch.float16) == "window"
-        y = torch.empty((Nb, Co, H, W), dtype=torch.float16, device="cuda")
-        xd = to_device(base, "f16").repeat(Nb // 64, 1, 1, 1)
-        mmact.mmact_conv2d(xd, to_device(w, "f16"), fp32_to_device(bias), y, st, pd, dl, "tanh")
-        del xd
+    if layout.startswith("nchw"):
+        # the tensor-memory im2col kernel by default; the window producer when it is turned off
+        mmact.mmact_set_conv_tmem(1 if layout == "nchw_window" else 0)
+        try:
+            assert mmact.mmact_conv2d_producer(Nb, C, H, W, Co, 3, 3, st, pd, dl, torch.float16,
+                                               torch.float16) == ("window" if layout == "nchw_window" else "tmem")
+            y = torch.empty((Nb, Co, H, W), dtype=torch.float16, device="cuda")
+            xd = to_device(base, "f16").repeat(Nb // 64, 1, 1, 1)
+            mmact.mmact_conv2d(xd, to_device(w, "f16"), fp32_to_device(bias), y, st, pd, dl, "tanh")
+            del xd
+        finally:
+            mmact.mmact_set_conv_tmem(0)
         got = sampled(y, pts)
     else:
         xd = to_device(base, "f16").permute(0, 2, 3, 1).contiguous().repeat(Nb // 64, 1, 1, 1)

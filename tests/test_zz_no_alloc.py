@@ -55,6 +55,46 @@ def test_noalloc_matches_split_entry_point_on_two_calls(lib):
         check(host(got), host(ref), cd, f"no-alloc call {call + 1}")
 
 
+def test_noalloc_at_its_size_limit_matches_split_entry_point(lib):
+    # M*N == MMACT_NOALLOC_MAX_ELEMENTS uses every element of the scratch array
+    M = N = 2048
+    assert M * N == mmact.NOALLOC_MAX_ELEMENTS
+    rng = np.random.default_rng(610)
+    A = to_device(synth.to_codes(rng.uniform(-1, 1, (M, 128)), "bf16"), "bf16")
+    B = to_device(synth.to_codes(rng.uniform(-1, 1, (128, N)), "bf16"), "bf16")
+    bias = fp32_to_device(rng.uniform(-1, 1, N).astype(np.float32))
+    ref = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty((M * N,), dtype=torch.float32, device="cuda")
+    mmact.mmact_gemm_split(A, B, bias, ref, ws, "sigmoid", 0.0)
+    got = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    assert _call_noalloc(lib, A, B, bias, got, "sigmoid", 0.0) == mmact.MMACT_OK
+    assert mmact.mmact_get_last_error() == mmact.MMACT_OK
+    check(host(got), host(ref), "f32", "no-alloc at the limit")
+    # one past the limit is refused before anything runs
+    C = torch.zeros((2048, 2056), dtype=torch.bfloat16, device="cuda")
+    B2 = torch.zeros((128, 2056), dtype=torch.bfloat16, device="cuda")
+    assert _call_noalloc(lib, A, B2, None, C, "relu", 0.0) == mmact.MMACT_ERR_UNSUPPORTED
+
+
+def test_noalloc_skinny_split_k_shape_matches_oracle(lib):
+    # 128 x 4096 x 4096: few output tiles and a long K loop, so the first kernel
+    # is the split-K cluster kernel when the device fits its clusters
+    import oracle
+    M, N, K = 128, 4096, 4096
+    rng = np.random.default_rng(611)
+    a = synth.to_codes(rng.uniform(-1, 1, (M, K)), "bf16")
+    b = synth.to_codes(rng.uniform(-1, 1, (K, N)), "bf16")
+    bias = rng.uniform(-1, 1, N).astype(np.float32)
+    split_k = mmact.mmact_gemm_split_k_choice(M, N, K)
+    got = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert _call_noalloc(lib, to_device(a, "bf16"), to_device(b, "bf16"), fp32_to_device(bias), got,
+                         "leaky_relu", 0.2) == mmact.MMACT_OK
+    assert mmact.mmact_get_last_error() == mmact.MMACT_OK
+    ref = oracle.get().gemm(a, b, "bf16", bias, "leaky_relu", 0.2)
+    check(host(got), ref, "bf16", f"no-alloc skinny (split-K factor {split_k})")
+    assert split_k == 4      # 16 tiles of 128 x 256, 64 K blocks: clusters of 4 on a GB300
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
     # rejected on the host before anything is enqueued
     A = torch.zeros((2048, 64), dtype=torch.bfloat16, device="cuda")
