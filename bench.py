@@ -201,18 +201,20 @@ def workload_bytes(mmact, wl):
             ob * wl.N * wl.Co * Ho * Wo)
 
 
-def roofline_record(flops, alg_bytes, ms, peaks, peak_src, tf32=False):
+def roofline_record(flops, alg_bytes, ms, peaks, peak_src, tf32=False, passes=1):
     """The roofline object for one launch of `ms` milliseconds: tensor-bound when the workload's
     arithmetic intensity (algorithmic flops per algorithmic byte) is at or above the ridge point
     of the two measured peaks, else HBM-bound on algorithmic bytes.  The tensor peak is the
-    measured cuBLAS bf16 burst figure (for tf32 operands half of it, the nominal ratio)."""
-    tpeak = peaks["bf16_tflops"] / (2.0 if tf32 else 1.0)
+    measured cuBLAS bf16 burst figure (for tf32 operands half of it, the nominal ratio; for split
+    precision a third of it: three bf16 products per multiply-add)."""
+    tpeak = peaks["bf16_tflops"] / (2.0 if tf32 else 1.0) / passes
     ridge = tpeak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if flops / alg_bytes >= ridge:
         tf = flops / (ms * 1e-3) / 1e12
         return {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s",
                 "frac": tf / tpeak,
-                "peak_source": f"{peak_src} burst bf16" + (" / 2 (tf32)" if tf32 else ""),
+                "peak_source": f"{peak_src} burst bf16" + (" / 2 (tf32)" if tf32 else "")
+                + (f" / {passes} (split precision)" if passes > 1 else ""),
                 "alg_bytes_per_launch": alg_bytes}
     gbs = alg_bytes / (ms * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -249,14 +251,14 @@ class NhwcProblem:
 
     layout = "nhwc"
 
-    def __init__(self, torch, mmact, wl, device, inputs=None, fp32_inputs=False):
-        self.mmact, self.wl = mmact, wl
+    def __init__(self, torch, mmact, wl, device, inputs=None, fp32_inputs=False, tf32=False):
+        self.mmact, self.wl, self.tf32 = mmact, wl, tf32
         inp = inputs if inputs is not None else wl.inputs()
         self.host = inp
         x = np.ascontiguousarray(inp["x"].transpose(0, 2, 3, 1))
         w = np.ascontiguousarray(inp["w"].transpose(0, 2, 3, 1))
         if fp32_inputs:
-            # the same values widened to fp32 (exact); the kernel runs them as tf32
+            # the same values widened to fp32 (exact); tf32 or split-precision arithmetic
             self.x = codes_to(torch, x, wl.dtype, device).float()
             self.w = codes_to(torch, w, wl.dtype, device).float()
         else:
@@ -272,7 +274,7 @@ class NhwcProblem:
     def run(self, variant="fused", stream=None):
         wl = self.wl
         self.mmact.mmact_conv2d_nhwc(self.x, self.w, self.bias, self.out, wl.stride, wl.pads,
-                                     wl.dilation, wl.act, wl.alpha, stream)
+                                     wl.dilation, wl.act, wl.alpha, stream, tf32=self.tf32)
 
 
 class Problem:
@@ -490,6 +492,8 @@ def main():
                     help="conv workloads: time the channels-last kernel (same values, transposed)")
     ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "persistent"],
                     help="GEMM workloads: the planner's kernel, or the one-SM persistent kernel")
+    ap.add_argument("--fusion-grid", action="store_true",
+                    help="time fused against two-kernel split over a grid of small shapes and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -515,6 +519,12 @@ def main():
     def barrier():
         if dist is not None:
             dist.barrier()
+
+    if args.fusion_grid:
+        if rank == 0:
+            print(json.dumps({"fusion_grid": fusion_grid(torch, mmact, device, torch.cuda.current_stream())}),
+                  flush=True)
+        return 0
 
     wl = synth.WORKLOADS[args.workload]
     if args.layout == "nhwc" and wl.kind == "conv":
@@ -766,6 +776,79 @@ def host_link(torch, hosts, devs, hout, dout, s_up, s_down, reps=6):
             "what": "pinned host buffers, one step's inputs up and its output down, no kernel"}
 
 
+# Shapes of the fused-versus-split grid: small contraction lengths (where the
+# epilogue is large relative to the main loop), tiny problems, and small-channel
+# convolutions -- the region where the fused_matmul_relu article reports that
+# fusing the activation into the matmul can lose ("64x64x64, batch 1024").
+GRID_GEMM_MN = (64, 256, 1024, 4096, 8192)
+GRID_GEMM_K = (64, 128, 256, 512, 1024)
+GRID_ACTS = ("relu", "tanh", "gelu")
+GRID_CONV = [  # (N, C, H, W, Co, k, stride, pad)
+    (8, 16, 56, 56, 64, 1, 1, 0), (8, 16, 56, 56, 64, 3, 1, 1), (8, 32, 56, 56, 128, 1, 1, 0),
+    (8, 32, 56, 56, 128, 3, 1, 1), (8, 64, 28, 28, 128, 1, 2, 0), (32, 16, 32, 32, 32, 3, 1, 1),
+]
+
+
+def fusion_grid(torch, mmact, device, stream, reps=20):
+    """Fused single kernel against the two-kernel split (fp32 workspace, then the activation pass)
+    on every grid shape: per-call time of each (CUDA-graph replay of `reps` back-to-back calls)
+    and split_over_fused = split time / fused time (> 1: fused faster)."""
+    rows = []
+    rng = np.random.default_rng(11)
+
+    def t(fn, n=reps):
+        return time_graph(torch, fn, n, stream)
+
+    for K in GRID_GEMM_K:
+        for M in GRID_GEMM_MN:
+            for N in GRID_GEMM_MN:
+                A = torch.from_numpy(rng.uniform(-1, 1, (M, K)).astype(np.float32)).to(device).bfloat16()
+                B = torch.from_numpy(rng.uniform(-1, 1, (K, N)).astype(np.float32)).to(device).bfloat16()
+                bias = torch.zeros(N, dtype=torch.float32, device=device)
+                C = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+                ws = torch.empty((M * N,), dtype=torch.float32, device=device)
+                for act in GRID_ACTS:
+                    f = t(lambda: mmact.mmact_gemm(A, B, bias, C, act, 0.0))
+                    sp = t(lambda: mmact.mmact_gemm_split(A, B, bias, C, ws, act, 0.0))
+                    rows.append({"kind": "gemm", "M": M, "N": N, "K": K, "act": act,
+                                 "fused_us": round(f * 1e3, 3), "split_us": round(sp * 1e3, 3),
+                                 "split_over_fused": round(sp / f, 3)})
+                del A, B, C, ws
+    # the article's counter-example: 64 x 64 x 64, 1024 independent problems, one call each
+    nb = 1024
+    As = torch.from_numpy(rng.uniform(-1, 1, (nb, 64, 64)).astype(np.float32)).to(device).bfloat16()
+    Bs = torch.from_numpy(rng.uniform(-1, 1, (nb, 64, 64)).astype(np.float32)).to(device).bfloat16()
+    Cs = torch.empty((nb, 64, 64), dtype=torch.bfloat16, device=device)
+    wss = torch.empty((nb, 64 * 64), dtype=torch.float32, device=device)
+    bias = torch.zeros(64, dtype=torch.float32, device=device)
+    for act in GRID_ACTS:
+        f = t(lambda: [mmact.mmact_gemm(As[i], Bs[i], bias, Cs[i], act, 0.0) for i in range(nb)], 1) / nb
+        sp = t(lambda: [mmact.mmact_gemm_split(As[i], Bs[i], bias, Cs[i], wss[i], act, 0.0) for i in range(nb)],
+               1) / nb
+        rows.append({"kind": "gemm_batch", "M": 64, "N": 64, "K": 64, "batch": nb, "act": act,
+                     "fused_us": round(f * 1e3, 3), "split_us": round(sp * 1e3, 3),
+                     "split_over_fused": round(sp / f, 3)})
+    del As, Bs, Cs, wss
+    for (Nb, C, H, W, Co, k, st, pd) in GRID_CONV:
+        x = torch.from_numpy(rng.normal(0, 1, (Nb, C, H, W)).astype(np.float32)).to(device).half()
+        w = torch.from_numpy(rng.normal(0, (1.0 / (C * k * k)) ** 0.5, (Co, C, k, k)).astype(np.float32)).to(device).half()
+        bias = torch.zeros(Co, dtype=torch.float32, device=device)
+        Ho, Wo = mmact.mmact_conv2d_out_shape(H, W, k, k, (st, st), (pd,) * 4, (1, 1))
+        y = torch.empty((Nb, Co, Ho, Wo), dtype=torch.float16, device=device)
+        ws = torch.empty((y.numel(),), dtype=torch.float32, device=device)
+        for act in GRID_ACTS:
+            f = t(lambda: mmact.mmact_conv2d(x, w, bias, y, (st, st), (pd,) * 4, (1, 1), act))
+            sp = t(lambda: mmact.mmact_conv2d_split(x, w, bias, y, ws, (st, st), (pd,) * 4, (1, 1), act))
+            rows.append({"kind": "conv", "N": Nb, "C": C, "H": H, "W": W, "Co": Co, "k": k, "stride": st,
+                         "act": act, "fused_us": round(f * 1e3, 3), "split_us": round(sp * 1e3, 3),
+                         "split_over_fused": round(sp / f, 3)})
+        del x, w, y, ws
+    st_ = mmact.mmact_get_last_error()
+    return {"rows": rows, "status": mmact.mmact_status_string(st_),
+            "split_faster": [r for r in rows if r["split_over_fused"] < 1.0],
+            "timing": f"CUDA graph of {reps} back-to-back calls (the batch row: 1024 calls), replayed 3 times"}
+
+
 def sweep(torch, mmact, device, stream, peaks):
     """Every workload, fused and two-kernel split: ms, TFLOP/s, % of peak, algorithmic GB/s."""
     out = {}
@@ -775,9 +858,9 @@ def sweep(torch, mmact, device, stream, peaks):
         nbytes = workload_bytes(mmact, wl)
         rec = {"timing": "CUDA graph of 20 back-to-back calls, replayed 3 times"}
         variants = ("fused", "split") + (("fused_residual",) if wl.kind == "gemm" else ())
-        def row(ms, nb=nbytes, tf32=False):
+        def row(ms, nb=nbytes, tf32=False, passes=1):
             tf = flops / (ms * 1e-3) / 1e12
-            rl = roofline_record(flops, nb, ms, peaks, "measured", tf32=tf32)
+            rl = roofline_record(flops, nb, ms, peaks, "measured", tf32=tf32, passes=passes)
             return {"ms": round(ms, 5), "tflops": round(tf, 2),
                     "pct_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 2),
                     "alg_gbs": round(nb / (ms * 1e-3) / 1e9, 1),
@@ -823,13 +906,26 @@ def sweep(torch, mmact, device, stream, peaks):
             nprob = NhwcProblem(torch, mmact, wl, device, inputs=prob.host)
             rec["fused_nhwc"] = row(time_graph(torch, lambda: nprob.run(), 20, stream))
             del nprob
-            # fp32 inputs (same values), tf32 tensor-core arithmetic; peak: nominal tf32 = bf16 / 2
-            fprob = NhwcProblem(torch, mmact, wl, device, inputs=prob.host, fp32_inputs=True)
-            ms = time_graph(torch, lambda: fprob.run(), 20, stream)
-            # fp32 inputs double the input bytes
+            # fp32 inputs (same values): one-pass tf32 (peak: nominal tf32 = bf16 / 2), and split
+            # precision (three bf16 products per multiply-add), channels-last and NCHW
             x_w = nbytes - 4.0 * wl.Co - (4 if wl.out_dtype == "f32" else 2) * prob.out.numel()
-            rec["fused_nhwc_fp32_inputs"] = row(ms, nbytes + x_w, tf32=True)
-            del fprob
+            for key, tf32 in (("fused_nhwc_tf32", True), ("fused_nhwc_fp32_split", False)):
+                fprob = NhwcProblem(torch, mmact, wl, device, inputs=prob.host, fp32_inputs=True, tf32=tf32)
+                ms = time_graph(torch, lambda: fprob.run(), 20, stream)
+                rec[key] = row(ms, nbytes + x_w, tf32=tf32, passes=1 if tf32 else 3)
+                del fprob
+            xf, wf = prob.x.float(), prob.w.float()
+            ms = time_graph(torch, lambda: mmact.mmact_conv2d(xf, wf, prob.bias, prob.out, wl.stride, wl.pads,
+                                                             wl.dilation, wl.act, wl.alpha), 20, stream)
+            rec["fused_fp32_split"] = row(ms, nbytes + x_w, passes=3)
+            del xf, wf
+        if wl.kind == "gemm" and wl.M * wl.N * wl.K < 2 ** 38:
+            # fp32 A and B (same values), split precision through the general kernel
+            Af, Bf = prob.A.float(), prob.B.float()
+            ms = time_graph(torch, lambda: mmact.mmact_gemm(Af, Bf, prob.bias, prob.out, wl.act, wl.alpha), 20,
+                            stream)
+            rec["fused_fp32_split"] = row(ms, nbytes + 2.0 * (wl.M * wl.K + wl.K * wl.N), passes=3)
+            del Af, Bf
         st = mmact.mmact_get_last_error()
         rec["status"] = mmact.mmact_status_string(st)
         out[wl.name] = rec

@@ -91,12 +91,12 @@ int out_kind(mmact_dtype d)
 {
     return d == MMACT_BF16 ? OUT_BF16 : (d == MMACT_F16 ? OUT_F16 : OUT_F32);
 }
-int elem_bytes(mmact_dtype d) { return d == MMACT_F32 ? 4 : 2; }
+int elem_bytes(mmact_dtype d) { return (d == MMACT_F32 || d == MMACT_TF32) ? 4 : 2; }
 CUtensorMapDataType tmap_type(mmact_dtype d)
 {
     return d == MMACT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                            : (d == MMACT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32);   // F32, TF32
 }
 
 // Tiled map over a row-major tensor given innermost-first dims (elements) and
@@ -203,6 +203,10 @@ bool choose_pair(const DeviceInfo &dev, int64_t M, int64_t N, int64_t num_kb, bo
     return pair_waves <= waves;
 }
 
+mmact_status conv_f32_gemm_enqueue(const void *A, const void *B, const float *bias, void *C, int64_t M,
+                                   int64_t N, int64_t K, mmact_dtype cd, mmact_act act, float alpha,
+                                   cudaStream_t stream, const void *res, const DeviceInfo *dev);
+
 // Shared by mmact_gemm, mmact_gemm_residual and the first kernel of
 // mmact_gemm_split.  `res`: residual [M, N] in the output dtype, or null.
 mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void *C, int64_t M,
@@ -216,6 +220,7 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
         cudaError_t e = launch_bias_act(bias, C, M, N, 0, N, out_kind(cd), (int)act, alpha, stream, res);
         return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
     }
+    if (ab == MMACT_F32) return conv_f32_gemm_enqueue(A, B, bias, C, M, N, K, cd, act, alpha, stream, res, dev);
     GemmLaunch L;
     std::memset(&L, 0, sizeof(L));
     const int tiles_m = (int)((M + 127) / 128);
@@ -298,10 +303,10 @@ mmact_status conv_geom(int64_t H, int64_t W, int64_t kh, int64_t kw, const int32
 mmact_status conv_check(const void *x, const void *w, const float *bias, const void *y, int64_t N,
                         int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
                         const int32_t *st, const int32_t *pd, const int32_t *dl, mmact_dtype in,
-                        mmact_dtype out, mmact_act act, ConvGeom *g, bool f32_in = false)
+                        mmact_dtype out, mmact_act act, ConvGeom *g, bool tf32_in = false)
 {
     if (N < 0 || C < 0 || Co < 0) return MMACT_ERR_INVALID_ARG;
-    const bool in_ok = valid_in(in) || (f32_in && in == MMACT_F32);
+    const bool in_ok = valid_in(in) || in == MMACT_F32 || (tf32_in && in == MMACT_TF32);
     if (!in_ok || !valid_out(out) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
     mmact_status s = conv_geom(H, W, kh, kw, st, pd, dl, g);
     if (s != MMACT_OK) return s;
@@ -350,8 +355,10 @@ void conv_plan(int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t k
     a.num_kb = (a.K + 63) / 64;
     a.ab_bf16 = in == MMACT_BF16 ? 1 : 0;
     a.out_elem_bytes = elem_bytes(out);
-    a.a_tma = (a.K % 8 == 0) ? 1 : 0;
+    a.f32 = in == MMACT_F32 ? 1 : 0;
+    a.a_tma = (a.K % 8 == 0 && !a.f32) ? 1 : 0;
     a.y_tma = ((P * a.out_elem_bytes) % 16 == 0) ? 1 : 0;
+    if (a.f32) return;   // fp32 inputs: the general gather producer, split precision
     // Vectorised producer: whole 16-byte input chunks per row (W % 8 == 0),
     // horizontal stride 1 or 2, filter by TMA, and an output TMA store:
     // 8 x 32 tiles when the output is exactly 32 wide (256 consecutive
@@ -396,6 +403,60 @@ void conv_plan(int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t k
         a.rowmul = hstride ? 1 : a.sh;
         a.raw_bytes = (int)raw;
     }
+}
+
+// An fp32 GEMM C[M,N] = act(A[M,K] B[K,N] + bias) run by the general conv
+// kernel in split precision as the 1x1 conv w = A ([M, K, 1, 1]), x = B ([1, K,
+// 1, N]): output channels are the rows of C, output pixels its columns, and
+// the bias runs along the columns.
+mmact_status conv_f32_gemm_enqueue(const void *A, const void *B, const float *bias, void *C, int64_t M,
+                                   int64_t N, int64_t K, mmact_dtype cd, mmact_act act, float alpha,
+                                   cudaStream_t stream, const void *res, const DeviceInfo *dev)
+{
+    if (M > MAX_DIM || N * M > ((int64_t)1 << 62)) return MMACT_ERR_UNSUPPORTED;
+    ConvLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    ConvArgs &a = L.args;
+    a.Nb = 1;
+    a.C = (int)K;
+    a.H = 1;
+    a.W = (int)N;
+    a.Co = (int)M;
+    a.kh = a.kw = 1;
+    a.sh = a.sw = 1;
+    a.dh = a.dw = 1;
+    a.Ho = 1;
+    a.Wo = (int)N;
+    a.P = (int)N;
+    a.K = (int)K;
+    a.tiles_co = (int)((M + 127) / 128);
+    a.tiles_p = (int)((N + 127) / 128);
+    if ((int64_t)a.tiles_co * a.tiles_p > MAX_DIM) return MMACT_ERR_UNSUPPORTED;
+    a.num_tiles = a.tiles_co * a.tiles_p;
+    a.num_kb = (int)((K + 63) / 64);
+    a.f32 = 1;
+    a.bias_col = 1;
+    a.out_elem_bytes = elem_bytes(cd);
+    a.y_tma = ((N * a.out_elem_bytes) % 16 == 0) ? 1 : 0;
+    a.act = (int)act;
+    a.alpha = alpha;
+    a.x = static_cast<const uint16_t *>(B);
+    a.w = static_cast<const uint16_t *>(A);
+    a.bias = bias;
+    a.res = res;
+    a.y = C;
+    a.status = dev->status;
+    a.wait_ns = g_wait_ns.load();
+    L.out = out_kind(cd);
+    L.grid = (int)std::min<int64_t>(a.num_tiles, dev->sm_count);
+    if (a.y_tma) {
+        const int e = a.out_elem_bytes;
+        const uint64_t d[3] = {(uint64_t)N, (uint64_t)M, 1};
+        const uint64_t sb[2] = {(uint64_t)N * e, (uint64_t)M * N * e};
+        const uint32_t bx[3] = {(uint32_t)(128 / e), 32, 1};
+        if (!encode(&L.tmY, cd, 3, C, d, sb, bx)) return MMACT_ERR_CUDA;
+    }
+    return launch_conv(L, stream) == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
 }
 
 int64_t gcd64(int64_t a, int64_t b)
@@ -612,6 +673,26 @@ mmact_status nhwc_enqueue(const void *x, const void *w, const float *bias, void 
         cudaError_t e = launch_bias_act(bias, y, M, Co, 0, Co, out_kind(out), (int)act, alpha, stream, res);
         return e == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
     }
+    if (in == MMACT_F32) {
+        // fp32 inputs to fp32 accuracy: the general gather kernel in split precision, channels-last
+        ConvLaunch CL;
+        std::memset(&CL, 0, sizeof(CL));
+        conv_plan(N, C, H, W, Co, kh, kw, st, pd, dl, g, in, out, CL.args);
+        ConvArgs &c = CL.args;
+        c.nhwc = 1;
+        c.y_tma = 0;
+        c.act = (int)act;
+        c.alpha = alpha;
+        c.x = static_cast<const uint16_t *>(x);
+        c.w = static_cast<const uint16_t *>(w);
+        c.bias = bias;
+        c.y = y;
+        c.status = dev->status;
+        c.wait_ns = g_wait_ns.load();
+        CL.out = out_kind(out);
+        CL.grid = (int)std::min<int64_t>(c.num_tiles, dev->sm_count);
+        return launch_conv(CL, stream) == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
+    }
     NhwcLaunch L;
     std::memset(&L, 0, sizeof(L));
     NhwcArgs &a = L.args;
@@ -631,7 +712,7 @@ mmact_status nhwc_enqueue(const void *x, const void *w, const float *bias, void 
     a.Ho = (int)g.Ho;
     a.Wo = (int)g.Wo;
     a.M = (int)M;
-    a.tf32 = in == MMACT_F32 ? 1 : 0;
+    a.tf32 = in == MMACT_TF32 ? 1 : 0;
     const int ie = elem_bytes(in);              // 2, or 4 for fp32 inputs
     a.kc = 128 / ie;                            // one 128-byte row of K per block
     a.ncb = (int)((C + a.kc - 1) / a.kc);
@@ -690,6 +771,46 @@ mmact_status nhwc_enqueue(const void *x, const void *w, const float *bias, void 
     return launch_conv_nhwc(L, stream) == cudaSuccess ? MMACT_OK : MMACT_ERR_CUDA;
 }
 
+// Fused single kernel or two-kernel split: the fused_matmul_relu article's
+// run-time decision (fuse, or fall back to the matmul and a separate
+// activation through a device temporary), decided here from a measured
+// fused-versus-split grid on GB300 (GEMMs with K from 64 to 1024 and M, N
+// from 64 to 8192, small-channel convs; every activation) rather than from
+// an on-chip buffer budget.  The fused kernel wins on every shape with ReLU,
+// LeakyReLU, tanh and sigmoid (1.2x to 3.4x) and on every GEMM with GELU
+// whose output has more than 64 Ki elements (1.07x to 1.57x).  The split path
+// wins (a) with GELU on a small output (M*N <= 64 Ki: one or two tiles, where
+// the fused epilogue's few warps are latency-bound on the activation and the
+// split's activation pass spreads over the whole GPU; 64x64x64: 4.8 against
+// 5.7 us) and on small-channel convs with GELU (C*kh*kw <= 288, Co >= 64:
+// up to 10 %); and (b) for an NCHW conv whose fused kernel would store its
+// 16-bit output element by element (neither the tensor-memory nor the
+// vectorised producer applies and the output row pitch rules out TMA
+// stores), where the split's fp32 intermediate is stored by TMA (1x1
+// stride 2 on 28 x 28: 8.4 against 16.8 us).
+constexpr int64_t SPLIT_GELU_MAX_OUTPUT = 65536;
+constexpr int64_t SPLIT_GELU_MAX_CONV_K = 288;
+
+bool gemm_prefers_split(int64_t M, int64_t N, int64_t K, mmact_dtype ab, mmact_act act)
+{
+    if (M == 0 || N == 0 || K == 0 || ab == MMACT_F32) return false;
+    return act == MMACT_ACT_GELU && M * N <= SPLIT_GELU_MAX_OUTPUT;
+}
+
+bool conv_prefers_split(int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co, int64_t kh, int64_t kw,
+                        const int32_t *st, const int32_t *pd, const int32_t *dl, const ConvGeom &g,
+                        mmact_dtype in, mmact_dtype out, mmact_act act)
+{
+    if (N == 0 || Co == 0 || C == 0 || in == MMACT_F32) return false;
+    if (act == MMACT_ACT_GELU && C * kh * kw <= SPLIT_GELU_MAX_CONV_K && Co >= 64) return true;
+    TmemConvArgs tp;
+    int bn = 0;
+    if (use_tconv() && tconv_plan(N, C, H, W, Co, kh, kw, st, pd, dl, g, in, tp, bn)) return false;
+    ConvArgs a;
+    conv_plan(N, C, H, W, Co, kh, kw, st, pd, dl, g, in, out, a);
+    return !a.vec && !a.y_tma;
+}
+
 // R is read element by element before the same element of the output is
 // written, so R == out is allowed; any other overlap is not.
 mmact_status residual_check(const void *R, const void *out, int64_t bytes)
@@ -713,8 +834,15 @@ mmact_status gemm_check(const void *A, const void *B, const float *bias, const v
     // a pointer may be null only when its tensor is empty
     if ((A == nullptr && M * K != 0) || (B == nullptr && K * N != 0) || (C == nullptr && M * N != 0))
         return MMACT_ERR_INVALID_ARG;
-    if (!valid_in(ab) || !valid_out(cd) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
+    const bool in_ok = valid_in(ab) || ab == MMACT_F32 || ab == MMACT_TF32;
+    if (!in_ok || !valid_out(cd) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
     if (bias != nullptr && !aligned4(bias)) return MMACT_ERR_INVALID_ARG;
+    if (ab == MMACT_TF32) return MMACT_ERR_UNSUPPORTED;   // one-pass tf32: channels-last conv only
+    if (ab == MMACT_F32) {
+        // fp32 operands are gathered element by element: 4-byte alignment, any K and N
+        if (!aligned4(A) || !aligned4(B) || !aligned16(C)) return MMACT_ERR_UNSUPPORTED;
+        return MMACT_OK;
+    }
     if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return MMACT_ERR_UNSUPPORTED;
     if (K % 8 != 0 || N % 8 != 0) return MMACT_ERR_UNSUPPORTED;
     return MMACT_OK;
@@ -775,6 +903,29 @@ MMACT_EXPORT mmact_status mmact_gemm_split(const void *A, const void *B, const f
                : MMACT_ERR_CUDA;
 }
 
+MMACT_EXPORT mmact_status mmact_gemm_auto_choice(int64_t M, int64_t N, int64_t K, mmact_dtype ab_dtype,
+                                                 mmact_dtype c_dtype, mmact_act act, int *split)
+{
+    if (split == nullptr || M < 0 || N < 0 || K < 0) return MMACT_ERR_INVALID_ARG;
+    const bool in_ok = valid_in(ab_dtype) || ab_dtype == MMACT_F32;
+    if (!in_ok || !valid_out(c_dtype) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
+    *split = gemm_prefers_split(M, N, K, ab_dtype, act) ? 1 : 0;
+    return MMACT_OK;
+}
+
+MMACT_EXPORT mmact_status mmact_gemm_auto(const void *A, const void *B, const float *bias, void *C,
+                                          int64_t M, int64_t N, int64_t K, mmact_dtype ab_dtype,
+                                          mmact_dtype c_dtype, mmact_act act, float alpha,
+                                          float *workspace, void *stream)
+{
+    mmact_status s = gemm_check(A, B, bias, C, M, N, K, ab_dtype, c_dtype, act);
+    if (s != MMACT_OK) return s;
+    if (workspace != nullptr && !aligned16(workspace)) return MMACT_ERR_UNSUPPORTED;
+    if (workspace != nullptr && gemm_prefers_split(M, N, K, ab_dtype, act))
+        return mmact_gemm_split(A, B, bias, C, M, N, K, ab_dtype, c_dtype, act, alpha, workspace, stream);
+    return mmact_gemm(A, B, bias, C, M, N, K, ab_dtype, c_dtype, act, alpha, stream);
+}
+
 MMACT_EXPORT mmact_status mmact_conv2d(const void *x, const void *w, const float *bias, void *y,
                                        int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co,
                                        int64_t kh, int64_t kw, const int32_t strides[2],
@@ -822,6 +973,7 @@ MMACT_EXPORT mmact_status mmact_conv2d_nhwc_residual(const void *x, const void *
     if (s != MMACT_OK) return s;
     if ((C * elem_bytes(in_dtype)) % 16 != 0 || Co % 8 != 0) return MMACT_ERR_UNSUPPORTED;
     if (N * g.Ho * g.Wo > MAX_DIM) return MMACT_ERR_UNSUPPORTED;
+    if (in_dtype == MMACT_F32) return MMACT_ERR_UNSUPPORTED;   // split precision: no channels-last residual
     s = residual_check(R, y, N * Co * g.Ho * g.Wo * elem_bytes(out_dtype));
     if (s != MMACT_OK) return s;
     return nhwc_enqueue(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations, g, in_dtype,
@@ -872,6 +1024,44 @@ MMACT_EXPORT mmact_status mmact_conv2d_nhwc(const void *x, const void *w, const 
                         out_dtype, act, alpha, static_cast<cudaStream_t>(stream));
 }
 
+MMACT_EXPORT mmact_status mmact_conv2d_auto_choice(int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co,
+                                                   int64_t kh, int64_t kw, const int32_t strides[2],
+                                                   const int32_t pads[4], const int32_t dilations[2],
+                                                   mmact_dtype in_dtype, mmact_dtype out_dtype, mmact_act act,
+                                                   int *split)
+{
+    if (split == nullptr || N < 0 || C < 0 || Co < 0) return MMACT_ERR_INVALID_ARG;
+    const bool in_ok = valid_in(in_dtype) || in_dtype == MMACT_F32;
+    if (!in_ok || !valid_out(out_dtype) || !valid_act(act)) return MMACT_ERR_INVALID_ARG;
+    ConvGeom g;
+    mmact_status s = conv_geom(H, W, kh, kw, strides, pads, dilations, &g);
+    if (s != MMACT_OK) return s;
+    if (C * H * W > MAX_DIM || Co * g.Ho * g.Wo > MAX_DIM || C * kh * kw > MAX_DIM) return MMACT_ERR_UNSUPPORTED;
+    *split = conv_prefers_split(N, C, H, W, Co, kh, kw, strides, pads, dilations, g, in_dtype, out_dtype, act)
+                 ? 1 : 0;
+    return MMACT_OK;
+}
+
+MMACT_EXPORT mmact_status mmact_conv2d_auto(const void *x, const void *w, const float *bias, void *y,
+                                            int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co,
+                                            int64_t kh, int64_t kw, const int32_t strides[2],
+                                            const int32_t pads[4], const int32_t dilations[2],
+                                            mmact_dtype in_dtype, mmact_dtype out_dtype, mmact_act act,
+                                            float alpha, float *workspace, void *stream)
+{
+    ConvGeom g;
+    mmact_status s = conv_check(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations,
+                                in_dtype, out_dtype, act, &g);
+    if (s != MMACT_OK) return s;
+    if (workspace != nullptr && !aligned16(workspace)) return MMACT_ERR_UNSUPPORTED;
+    if (workspace != nullptr &&
+        conv_prefers_split(N, C, H, W, Co, kh, kw, strides, pads, dilations, g, in_dtype, out_dtype, act))
+        return mmact_conv2d_split(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations, in_dtype,
+                                  out_dtype, act, alpha, workspace, stream);
+    return mmact_conv2d(x, w, bias, y, N, C, H, W, Co, kh, kw, strides, pads, dilations, in_dtype, out_dtype,
+                        act, alpha, stream);
+}
+
 MMACT_EXPORT mmact_status mmact_conv2d_out_shape(int64_t H, int64_t W, int64_t kh, int64_t kw,
                                                  const int32_t strides[2], const int32_t pads[4],
                                                  const int32_t dilations[2], int64_t *Ho,
@@ -892,7 +1082,8 @@ MMACT_EXPORT int mmact_conv2d_producer(int64_t N, int64_t C, int64_t H, int64_t 
                                        mmact_dtype in_dtype, mmact_dtype out_dtype)
 {
     ConvGeom g;
-    if (N < 0 || C <= 0 || Co < 0 || !valid_in(in_dtype) || !valid_out(out_dtype)) return -1;
+    if (N < 0 || C <= 0 || Co < 0 || !(valid_in(in_dtype) || in_dtype == MMACT_F32) || !valid_out(out_dtype))
+        return -1;
     if (conv_geom(H, W, kh, kw, strides, pads, dilations, &g) != MMACT_OK) return -1;
     if (C * H * W > MAX_DIM || Co * g.Ho * g.Wo > MAX_DIM || C * kh * kw > MAX_DIM) return -1;
     if (use_tconv()) {

@@ -23,17 +23,32 @@
 // aligned).  The article's stride-2 odd/even column split is not needed:
 // address generation handles any stride.
 //
+// fp32 inputs (F32): x and w are fp32 and are used to fp32 accuracy by
+// splitting each value v into bf16 hi = rn(v) and lo = rn(v - hi), so that
+// hi + lo carries 16 significant bits and x*w = xh*wh + xl*wh + xh*wl up to the
+// dropped xl*wl term (below 2^-16 of |x*w|) and the roundings of hi and lo
+// (about 2^-17 of |v| each).  The gather warps split both operands (the filter
+// is always gathered in this mode) into hi and lo tiles, and the MMA issuer
+// accumulates the three products per K step in the same fp32 TMEM
+// accumulator.  The same kernel runs an fp32 GEMM C[M,N] = A[M,K] B[K,N] as
+// the 1x1 conv w = A ([M, K, 1, 1]), x = B ([1, K, 1, N]), with the bias along
+// the output columns (bias_col), and channels-last fp32 convs (nhwc): x
+// [N,H,W,C] and the filter [Co,kh,kw,C] gathered with K = (r, q, ci), y
+// [N,Ho,Wo,Co] written with plain stores (the 32 lanes of a warp hold 32
+// consecutive output channels of one pixel).
+//
 // Warps: 0 filter TMA, 1 TMEM + MMA, 2..5 epilogue, 6..9 B-tile gather.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace mmact {
 
-struct ConvCfg {
+template <bool F32>
+struct ConvCfgT {
     static constexpr int BM = 128, BN = 128, BK = 64;
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BK * BN * 2;
-    static constexpr int STAGES = 6;
+    static constexpr int A_BYTES = BM * BK * 2 * (F32 ? 2 : 1);   // hi tile, then lo tile (F32)
+    static constexpr int B_BYTES = BK * BN * 2 * (F32 ? 2 : 1);
+    static constexpr int STAGES = F32 ? 3 : 6;
     static constexpr int EPI_BYTES = 4 * 2 * 4096;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int OFF_A = 0;
@@ -46,6 +61,7 @@ struct ConvCfg {
     static constexpr int THREADS = 320;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
+using ConvCfg = ConvCfgT<false>;
 
 // tile -> (image, pixel block, channel block); channel blocks vary fastest so
 // CTAs running side by side share the same input pixels in L2.
@@ -69,12 +85,21 @@ __device__ __forceinline__ uint32_t a_tile_offset(int m, int k)
     return (uint32_t)(m * 128 + ((((k >> 3) & 7) ^ (m & 7)) << 4) + ((k & 7) << 1));
 }
 
-template <int OUT>
-__global__ void __launch_bounds__(ConvCfg::THREADS, 1)
+// v = hi + lo with hi, lo bf16 (round to nearest even both times).
+__device__ __forceinline__ void split_bf16(float v, uint16_t &hi, uint16_t &lo)
+{
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    const __nv_bfloat16 l = __float2bfloat16_rn(v - __bfloat162float(h));
+    hi = *reinterpret_cast<const uint16_t *>(&h);
+    lo = *reinterpret_cast<const uint16_t *>(&l);
+}
+
+template <int OUT, bool F32>
+__global__ void __launch_bounds__(ConvCfgT<F32>::THREADS, 1)
     conv_act_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmY,
                     const ConvArgs p)
 {
-    using Cfg = ConvCfg;
+    using Cfg = ConvCfgT<F32>;
     constexpr int STAGES = Cfg::STAGES, BN = Cfg::BN;
     constexpr int COLS = OUT == OUT_F32 ? 32 : 64;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -104,7 +129,7 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
 
     if (threadIdx.x == 0) {
         // full: the 4 gather warps, plus the filter TMA producer when it is used
-        const uint32_t full_count = p.a_tma ? 5u : 4u;
+        const uint32_t full_count = (p.a_tma && !F32) ? 5u : 4u;
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(pp.full0 + 8 * s, full_count);
             ptx::mbar_init(pp.empty0 + 8 * s, 1);
@@ -130,7 +155,7 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
     const uint32_t sA = base + Cfg::OFF_A, sB = base + Cfg::OFF_B;
 
     if (warp == 0) {
-        if (lane == 0 && p.a_tma) {
+        if (lane == 0 && p.a_tma && !F32) {
             // ---------------------------------------------- filter producer --
             ptx::prefetch_tensormap(&tmW);
             uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;
@@ -154,9 +179,48 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
                     ptx::mbar_wait_bounded(pp.full0 + 8 * s, (last_par >> s) & 1u, DRAIN_NS, nullptr);
         }
     } else if (warp == 1) {
-        if (lane == 0)
-            mma_role<BN, STAGES, false, true>(pp, sA, sB, p.num_tiles, p.num_kb,
-                                              ptx::idesc_f16(p.ab_bf16 != 0, false, true, 128, BN));
+        if (lane == 0) {
+            if constexpr (F32) {
+                // split precision: per K step of 16, hi*hi + lo*hi + hi*lo (bf16 operands)
+                const uint32_t idesc = ptx::idesc_f16(true, false, true, 128, BN);
+                constexpr uint32_t AH = 128 * 64 * 2, BH = 64 * 128 * 2;   // offset of the lo tiles
+                uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+                bool ok = true;
+                for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+                    if (!pipe_wait(pp, pp.tempty0 + 8 * acc, acc_phase ^ 1u)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t d = pp.tmem + acc * BN;
+                    for (int kb = 0; kb < p.num_kb; ++kb) {
+                        if (!pipe_wait(pp, pp.full0 + 8 * stage, phase)) { ok = false; break; }
+                        ptx::fence_proxy_async_smem();
+                        ptx::tc_fence_after();
+                        const uint32_t a0 = sA + stage * Cfg::A_BYTES, b0 = sB + stage * Cfg::B_BYTES;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t ah = ptx::smem_desc(a0 + 32u * k, 16u, 1024u, ptx::SWIZZLE_128B);
+                            const uint64_t al = ptx::smem_desc(a0 + AH + 32u * k, 16u, 1024u, ptx::SWIZZLE_128B);
+                            const uint64_t bh = ptx::smem_desc(b0 + 2048u * k, 8192u, 1024u, ptx::SWIZZLE_128B);
+                            const uint64_t bl = ptx::smem_desc(b0 + BH + 2048u * k, 8192u, 1024u, ptx::SWIZZLE_128B);
+                            ptx::mma_f16(d, ah, bh, idesc, (kb | k) != 0 ? 1u : 0u);
+                            ptx::mma_f16(d, al, bh, idesc, 1u);
+                            ptx::mma_f16(d, ah, bl, idesc, 1u);
+                        }
+                        ptx::mma_commit(pp.empty0 + 8 * stage);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit(pp.tfull0 + 8 * acc);
+                    acc ^= 1u;
+                    if (acc == 0) acc_phase ^= 1u;
+                }
+                if (!ok) pipe_fail(pp);
+                ptx::mma_commit(pp.drain);
+                ptx::mbar_wait_bounded(pp.drain, 0, DRAIN_NS, nullptr);
+            } else {
+                mma_role<BN, STAGES, false, true>(pp, sA, sB, p.num_tiles, p.num_kb,
+                                                  ptx::idesc_f16(p.ab_bf16 != 0, false, true, 128, BN));
+            }
+        }
     } else if (warp >= 6) {
         // ---------------------------------------------------- B-tile gather --
         // Thread j owns pixel column j of every B tile.  For each stage it
@@ -181,6 +245,63 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
             // (ci, r, q) of the next K index, advanced one step per element
             int r = 0, q = 0, k = 0, cbase = 0;       // cbase = ci * H * W
             for (int kb = 0; kb < p.num_kb; ++kb) {
+                if constexpr (F32) {
+                    // fp32 values, split into hi and lo tiles (x, then the filter rows m = j)
+                    const float *xf = reinterpret_cast<const float *>(p.x) + (int64_t)n * p.C * HW;
+                    float xv[64];
+                    if (p.nhwc) {
+                        // K = (r, q, ci), channels fastest; cbase holds ci here
+#pragma unroll
+                        for (int kl = 0; kl < 64; ++kl) {
+                            const int ih = ih0 + r * p.dh, iw = iw0 + q * p.dw;
+                            const bool in = pvalid && k < p.K && (unsigned)ih < (unsigned)p.H &&
+                                            (unsigned)iw < (unsigned)p.W;
+                            xv[kl] = in ? __ldg(xf + ((int64_t)ih * p.W + iw) * p.C + cbase) : 0.0f;
+                            ++k;
+                            if (++cbase == p.C) {
+                                cbase = 0;
+                                if (++q == p.kw) { q = 0; ++r; }
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int kl = 0; kl < 64; ++kl) {
+                            const int ih = ih0 + r * p.dh, iw = iw0 + q * p.dw;
+                            const bool in = pvalid && k < p.K && (unsigned)ih < (unsigned)p.H &&
+                                            (unsigned)iw < (unsigned)p.W;
+                            xv[kl] = in ? __ldg(xf + cbase + ih * p.W + iw) : 0.0f;
+                            ++k;
+                            if (++q == p.kw) {
+                                q = 0;
+                                if (++r == p.kh) { r = 0; cbase += HW; }
+                            }
+                        }
+                    }
+                    if (!warp_pipe_wait(pp, pp.empty0 + 8 * stage, phase ^ 1u)) { ok = false; break; }
+                    const uint32_t bt = sB + stage * Cfg::B_BYTES;
+#pragma unroll
+                    for (int kl = 0; kl < 64; ++kl) {
+                        uint16_t hi, lo;
+                        split_bf16(xv[kl], hi, lo);
+                        ptx::st_shared_u16(bt + b_tile_offset(kl, j), hi);
+                        ptx::st_shared_u16(bt + 64 * 128 * 2 + b_tile_offset(kl, j), lo);
+                    }
+                    const uint32_t at = sA + stage * Cfg::A_BYTES;
+                    const float *wr = reinterpret_cast<const float *>(p.w) + (int64_t)(cb * 128 + j) * p.K;
+#pragma unroll 8
+                    for (int kl = 0; kl < 64; ++kl) {
+                        const int kk = kb * 64 + kl;
+                        const float v = (j < co_rows && kk < p.K) ? __ldg(wr + kk) : 0.0f;
+                        uint16_t hi, lo;
+                        split_bf16(v, hi, lo);
+                        ptx::st_shared_u16(at + a_tile_offset(j, kl), hi);
+                        ptx::st_shared_u16(at + 128 * 64 * 2 + a_tile_offset(j, kl), lo);
+                    }
+                    __syncwarp();   // the MMA thread fences the stores into the async proxy
+                    if (lane == 0) ptx::mbar_arrive(pp.full0 + 8 * stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    continue;
+                }
                 uint16_t vals[64];
 #pragma unroll
                 for (int kl = 0; kl < 64; ++kl) {
@@ -226,7 +347,7 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
             conv_tile(t, p, n, pb, cb);
             const int co_row0 = cb * 128 + qd * 32;
             const int co = co_row0 + lane;
-            const float brow = (p.bias != nullptr && co < p.Co) ? __ldg(p.bias + co) : 0.0f;
+            const float brow = (p.bias != nullptr && !p.bias_col && co < p.Co) ? __ldg(p.bias + co) : 0.0f;
             if (!warp_epi_wait(pp, pp.tfull0 + 8 * acc, acc_phase)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t tbase = pp.tmem + ((uint32_t)(qd * 32) << 16) + acc * BN;
@@ -242,8 +363,12 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
                            (((int64_t)n * p.Co + co) * p.P + pix0) * (OUT == OUT_F32 ? 4 : 2);
                     ptx::prefetch_l1(rrow);
                 }
-                epi_unit_dispatch<OUT, true>(p.act, tbase + u * COLS, nullptr, p.P - pix0, brow, p.alpha, buf,
-                                             lane, rrow, p.res != nullptr);
+                if (p.bias_col)          // a GEMM run as a 1x1 conv: bias along the output columns
+                    epi_unit_dispatch<OUT, false>(p.act, tbase + u * COLS, p.bias != nullptr ? p.bias + pix0 : nullptr,
+                                                  p.P - pix0, 0.0f, p.alpha, buf, lane, rrow, p.res != nullptr);
+                else
+                    epi_unit_dispatch<OUT, true>(p.act, tbase + u * COLS, nullptr, p.P - pix0, brow, p.alpha, buf,
+                                                 lane, rrow, p.res != nullptr);
                 if (p.y_tma) {
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
@@ -251,20 +376,44 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
                         ptx::tma_store_3d(&tmY, buf, pix0, co_row0, n);
                         ptx::bulk_commit();
                     }
+                } else if (!p.nhwc) {
+                    // plain stores, coalesced: for each of the unit's 32 channel rows the
+                    // lanes store consecutive pixels, read back from the swizzled staging rows
+                    __syncwarp();
+                    const int nvalid = min(COLS, p.P - pix0);
+                    const int ebytes = p.out_elem_bytes;
+                    const uint8_t *stage_rows = smem + (buf - base);
+                    for (int r = 0; r < 32 && co_row0 + r < p.Co; ++r) {
+                        uint8_t *dst = reinterpret_cast<uint8_t *>(p.y) +
+                                       (((int64_t)n * p.Co + co_row0 + r) * p.P + pix0) * ebytes;
+                        for (int e = lane; e < nvalid; e += 32) {
+                            const int byte = e * ebytes;
+                            const uint8_t *src = stage_rows + r * 128 + (((byte >> 4) ^ (r & 7)) << 4) + (byte & 15);
+                            if (ebytes == 4)
+                                *reinterpret_cast<uint32_t *>(dst + byte) = *reinterpret_cast<const uint32_t *>(src);
+                            else
+                                *reinterpret_cast<uint16_t *>(dst + byte) = *reinterpret_cast<const uint16_t *>(src);
+                        }
+                    }
+                    __syncwarp();
                 } else if (co < p.Co) {
-                    // plain stores of this thread's row segment, read back from its swizzled row
+                    // channels-last: each lane stores its channel for the segment's pixels (the
+                    // 32 lanes' channels are contiguous in y; pixel e is Co elements after e - 1)
                     const uint8_t *row = smem + (buf - base) + lane * 128;
+                    const int64_t pstride = p.nhwc ? (int64_t)p.Co * p.out_elem_bytes : p.out_elem_bytes;
                     uint8_t *dst = reinterpret_cast<uint8_t *>(p.y) +
-                                   (((int64_t)n * p.Co + co) * p.P + pix0) * p.out_elem_bytes;
+                                   (p.nhwc ? (((int64_t)n * p.P + pix0) * p.Co + co)
+                                           : (((int64_t)n * p.Co + co) * p.P + pix0)) * p.out_elem_bytes;
                     const int nvalid = min(COLS, p.P - pix0);
                     for (int e = 0; e < nvalid; ++e) {
                         const int byte = e * p.out_elem_bytes;
                         const int chunk = (byte >> 4) ^ (lane & 7);
                         const uint8_t *src = row + chunk * 16 + (byte & 15);
+                        uint8_t *d = dst + (int64_t)e * pstride;
                         if (p.out_elem_bytes == 4)
-                            *reinterpret_cast<uint32_t *>(dst + byte) = *reinterpret_cast<const uint32_t *>(src);
+                            *reinterpret_cast<uint32_t *>(d) = *reinterpret_cast<const uint32_t *>(src);
                         else
-                            *reinterpret_cast<uint16_t *>(dst + byte) = *reinterpret_cast<const uint16_t *>(src);
+                            *reinterpret_cast<uint16_t *>(d) = *reinterpret_cast<const uint16_t *>(src);
                     }
                     __syncwarp();
                 } else {
@@ -295,33 +444,44 @@ __global__ void __launch_bounds__(ConvCfg::THREADS, 1)
     }
 }
 
-template <int OUT>
+template <int OUT, bool F32>
 static cudaError_t launch_conv_t(const ConvLaunch &L, cudaStream_t stream)
 {
-    return launch_k(conv_act_kernel<OUT>, L.grid, ConvCfg::THREADS, ConvCfg::SMEM_BYTES, stream, L.tmW,
-                    L.tmY, L.args);
+    using Cfg = ConvCfgT<F32>;
+    return launch_k(conv_act_kernel<OUT, F32>, L.grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream, L.tmW, L.tmY,
+                    L.args);
+}
+
+template <int OUT, bool F32>
+static cudaError_t setup_conv_t()
+{
+    return cudaFuncSetAttribute(conv_act_kernel<OUT, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                ConvCfgT<F32>::SMEM_BYTES);
 }
 
 cudaError_t setup_conv_kernels()
 {
-    cudaError_t e = cudaFuncSetAttribute(conv_act_kernel<OUT_BF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         ConvCfg::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(conv_act_kernel<OUT_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 ConvCfg::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(conv_act_kernel<OUT_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 ConvCfg::SMEM_BYTES);
+    cudaError_t e = setup_conv_t<OUT_BF16, false>();
+    if (e == cudaSuccess) e = setup_conv_t<OUT_F16, false>();
+    if (e == cudaSuccess) e = setup_conv_t<OUT_F32, false>();
+    if (e == cudaSuccess) e = setup_conv_t<OUT_BF16, true>();
+    if (e == cudaSuccess) e = setup_conv_t<OUT_F16, true>();
+    if (e == cudaSuccess) e = setup_conv_t<OUT_F32, true>();
     return e;
 }
 
 cudaError_t launch_conv(const ConvLaunch &L, cudaStream_t stream)
 {
     if (L.args.vec) return launch_conv_vec(L, stream);
-    if (L.out == OUT_BF16) return launch_conv_t<OUT_BF16>(L, stream);
-    if (L.out == OUT_F16) return launch_conv_t<OUT_F16>(L, stream);
-    if (L.out == OUT_F32) return launch_conv_t<OUT_F32>(L, stream);
+    if (L.args.f32) {
+        if (L.out == OUT_BF16) return launch_conv_t<OUT_BF16, true>(L, stream);
+        if (L.out == OUT_F16) return launch_conv_t<OUT_F16, true>(L, stream);
+        if (L.out == OUT_F32) return launch_conv_t<OUT_F32, true>(L, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (L.out == OUT_BF16) return launch_conv_t<OUT_BF16, false>(L, stream);
+    if (L.out == OUT_F16) return launch_conv_t<OUT_F16, false>(L, stream);
+    if (L.out == OUT_F32) return launch_conv_t<OUT_F32, false>(L, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -50,6 +50,9 @@ struct ConvArgs {
     int raw_bytes;       //   bytes of one window
     int a_tma;           // 1: filter tiles by TMA, 0: gathered by the producer warps
     int y_tma;           // 1: output tiles by TMA store, 0: direct global stores
+    int f32;             // 1: fp32 x and w, each split into bf16 hi + lo (three MMAs per K step)
+    int bias_col;        // 1: bias per output pixel column (a GEMM run as a 1x1 conv), 0: per channel
+    int nhwc;            // 1 (with f32): channels-last x [N,H,W,C], filter [Co,kh,kw,C], y [N,Ho,Wo,Co]
     int out_elem_bytes;
     const uint16_t *x;
     const uint16_t *w;

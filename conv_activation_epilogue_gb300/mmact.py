@@ -20,6 +20,7 @@ LIBRARY = os.path.join(_HERE, "libmmact.so")
 MMACT_OK, MMACT_ERR_INVALID_ARG, MMACT_ERR_UNSUPPORTED, MMACT_ERR_CUDA, MMACT_ERR_TIMEOUT = range(5)
 ACT = {"none": 0, "relu": 1, "leaky_relu": 2, "tanh": 3, "sigmoid": 4, "gelu": 5}
 DTYPE = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
+MMACT_TF32 = 3   # fp32 inputs computed as tf32 (one pass); float32 tensors default to split precision
 
 _lib = None
 
@@ -32,6 +33,7 @@ SYMBOLS = [
     "mmact_set_wait_timeout_ns",
     "mmact_selftest_wait_timeout", "mmact_set_gemm_tile_n", "mmact_set_gemm_split_k",
     "mmact_gemm_split_k_choice", "mmact_set_gemm_pair", "mmact_gemm_kernel_choice", "mmact_set_conv_tmem",
+    "mmact_gemm_auto", "mmact_gemm_auto_choice", "mmact_conv2d_auto", "mmact_conv2d_auto_choice",
     "mmact_status_string", "mmact_version",
 ]
 
@@ -64,6 +66,14 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     conv = [vp, vp, vp, vp] + [i64] * 7 + [p_i32, p_i32, p_i32, ci, ci, ci, f32]
     L.mmact_conv2d.argtypes = conv + [vp]
     L.mmact_conv2d_split.argtypes = conv + [vp, vp]
+    L.mmact_conv2d_auto.argtypes = conv + [vp, vp]
+    L.mmact_conv2d_auto.restype = ci
+    L.mmact_conv2d_auto_choice.argtypes = [i64] * 7 + [p_i32, p_i32, p_i32, ci, ci, ci, ctypes.POINTER(ci)]
+    L.mmact_conv2d_auto_choice.restype = ci
+    L.mmact_gemm_auto.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, f32, vp, vp]
+    L.mmact_gemm_auto.restype = ci
+    L.mmact_gemm_auto_choice.argtypes = [i64, i64, i64, ci, ci, ci, ctypes.POINTER(ci)]
+    L.mmact_gemm_auto_choice.restype = ci
     L.mmact_conv2d_nhwc.argtypes = conv + [vp]
     L.mmact_conv2d_nhwc.restype = ci
     conv_res = [vp, vp, vp, vp, vp] + [i64] * 7 + [p_i32, p_i32, p_i32, ci, ci, ci, f32, vp]
@@ -125,7 +135,7 @@ def _dev(t: torch.Tensor, name: str, dtypes) -> int:
     return t.data_ptr()
 
 
-_IN = (torch.float16, torch.bfloat16)
+_IN = (torch.float16, torch.bfloat16, torch.float32)   # float32 inputs: split precision
 _OUT = (torch.float16, torch.bfloat16, torch.float32)
 
 
@@ -181,6 +191,28 @@ def mmact_gemm_split(A, B, bias, C, workspace, act: str = "none", alpha: float =
         raise ValueError("workspace must hold M*N fp32 elements")
     _check(L.mmact_gemm_split(pa, pb, pbias, pc, M, N, K, DTYPE[A.dtype], DTYPE[C.dtype], ACT[act],
                               float(alpha), pw, _stream_handle(stream)), "mmact_gemm_split")
+
+
+def mmact_gemm_auto(A, B, bias, C, act: str = "none", alpha: float = 0.0, workspace=None, stream=None) -> None:
+    """Fused or two-kernel GEMM, decided per shape (see include/mmact.h); the split path
+    needs `workspace` (fp32, at least M*N elements) and is never taken without one."""
+    L = load()
+    pa, pb, pbias, pc, M, N, K = _gemm_args(A, B, bias, C)
+    pw = None
+    if workspace is not None:
+        pw = _dev(workspace, "workspace", (torch.float32,))
+        if workspace.numel() < M * N:
+            raise ValueError("workspace must hold M*N fp32 elements")
+    _check(L.mmact_gemm_auto(pa, pb, pbias, pc, M, N, K, DTYPE[A.dtype], DTYPE[C.dtype], ACT[act],
+                             float(alpha), pw, _stream_handle(stream)), "mmact_gemm_auto")
+
+
+def mmact_gemm_auto_choice(M, N, K, ab_dtype, c_dtype, act: str) -> str:
+    """"split" or "fused": the path mmact_gemm_auto takes with a workspace (dtypes: torch dtypes)."""
+    out = ctypes.c_int(-1)
+    _check(load().mmact_gemm_auto_choice(int(M), int(N), int(K), DTYPE[ab_dtype], DTYPE[c_dtype], ACT[act],
+                                         ctypes.byref(out)), "mmact_gemm_auto_choice")
+    return "split" if out.value == 1 else "fused"
 
 
 NOALLOC_MAX_ELEMENTS = 4194304   # MMACT_NOALLOC_MAX_ELEMENTS in include/mmact.h
@@ -281,13 +313,46 @@ def mmact_conv2d_split(x, w, bias, y, workspace, stride=(1, 1), pads=(0, 0, 0, 0
                                 _stream_handle(stream)), "mmact_conv2d_split")
 
 
+def _in_code(x, tf32: bool) -> int:
+    if tf32:
+        if x.dtype != torch.float32:
+            raise ValueError("tf32=True needs float32 x and w")
+        return MMACT_TF32
+    return DTYPE[x.dtype]
+
+
+def mmact_conv2d_auto(x, w, bias, y, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1),
+                      act: str = "tanh", alpha: float = 0.0, workspace=None, stream=None) -> None:
+    """NCHW fused or two-kernel conv, decided per geometry (see include/mmact.h)."""
+    L = load()
+    args = _conv_args(x, w, bias, y, stride, pads, dilation)
+    pws = None
+    if workspace is not None:
+        pws = _dev(workspace, "workspace", (torch.float32,))
+        if workspace.numel() < y.numel():
+            raise ValueError("workspace must hold y.numel() fp32 elements")
+    _check(L.mmact_conv2d_auto(*args, DTYPE[x.dtype], DTYPE[y.dtype], ACT[act], float(alpha), pws,
+                               _stream_handle(stream)), "mmact_conv2d_auto")
+
+
+def mmact_conv2d_auto_choice(N, C, H, W, Co, kh, kw, stride, pads, dilation, in_dtype, out_dtype,
+                             act: str) -> str:
+    """"split" or "fused": the path mmact_conv2d_auto takes with a workspace."""
+    out = ctypes.c_int(-1)
+    _check(load().mmact_conv2d_auto_choice(N, C, H, W, Co, kh, kw, _i32(stride, 2), _i32(pads, 4),
+                                           _i32(dilation, 2), DTYPE[in_dtype], DTYPE[out_dtype], ACT[act],
+                                           ctypes.byref(out)), "mmact_conv2d_auto_choice")
+    return "split" if out.value == 1 else "fused"
+
+
 def mmact_conv2d_nhwc(x, w, bias, y, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1),
-                      act: str = "tanh", alpha: float = 0.0, stream=None) -> None:
+                      act: str = "tanh", alpha: float = 0.0, stream=None, tf32: bool = False) -> None:
     """Channels-last y = act(conv2d(x, w) + bias): x [N,H,W,C], w [Co,kh,kw,C], y [N,Ho,Wo,Co].
-    x and w may be fp32 (tf32 tensor-core arithmetic, see include/mmact.h)."""
+    float32 x and w run in split precision (fp32 accuracy), or as tf32 (one pass) with
+    tf32=True (see include/mmact.h)."""
     L = load()
     px, pw, pb, py, *rest = _nhwc_args(x, w, bias, y, stride, pads, dilation)
-    _check(L.mmact_conv2d_nhwc(px, pw, pb, py, *rest, DTYPE[x.dtype], DTYPE[y.dtype], ACT[act],
+    _check(L.mmact_conv2d_nhwc(px, pw, pb, py, *rest, _in_code(x, tf32), DTYPE[y.dtype], ACT[act],
                                float(alpha), _stream_handle(stream)), "mmact_conv2d_nhwc")
 
 
@@ -309,12 +374,12 @@ def _nhwc_args(x, w, bias, y, stride, pads, dilation):
 
 
 def mmact_conv2d_nhwc_residual(x, w, bias, R, y, stride=(1, 1), pads=(0, 0, 0, 0), dilation=(1, 1),
-                               act: str = "tanh", alpha: float = 0.0, stream=None) -> None:
+                               act: str = "tanh", alpha: float = 0.0, stream=None, tf32: bool = False) -> None:
     """Channels-last y = act(conv2d(x, w) + bias + R); R has y's shape [N,Ho,Wo,Co] and dtype."""
     L = load()
     px, pw, pb, py, *rest = _nhwc_args(x, w, bias, y, stride, pads, dilation)
     pr = _residual_ptr(R, y)
-    _check(L.mmact_conv2d_nhwc_residual(px, pw, pb, pr, py, *rest, DTYPE[x.dtype], DTYPE[y.dtype],
+    _check(L.mmact_conv2d_nhwc_residual(px, pw, pb, pr, py, *rest, _in_code(x, tf32), DTYPE[y.dtype],
                                         ACT[act], float(alpha), _stream_handle(stream)),
            "mmact_conv2d_nhwc_residual")
 

@@ -82,19 +82,35 @@ typedef enum {
 typedef enum {
     MMACT_F16 = 0,
     MMACT_BF16 = 1,
-    MMACT_F32 = 2
+    MMACT_F32 = 2,   /* as an input: fp32 values used to fp32 accuracy (split precision, below) */
+    MMACT_TF32 = 3   /* input only: fp32 values rounded to tf32 (10 fraction bits) by the tensor core */
 } mmact_dtype;
 
 /*
+ * fp32 inputs (the Fused ConvTanh article evaluates fp32 cases beside fp16 and
+ * bf16).  MMACT_F32 inputs are computed in split precision: every input value
+ * v is split into two bf16 values hi = rn(v) and lo = rn(v - hi), and each
+ * product as xh*wh + xl*wh + xh*wl (three tensor-core products accumulated in
+ * the same fp32 accumulator), which leaves an error of about 2^-15 of
+ * sum_k |x_k w_k| -- inside the fp32-output tolerance 2e-3 + 2e-3 |y|.  It
+ * runs on the general gather kernel (three MMAs per K step; several times
+ * slower than 16-bit inputs).  MMACT_TF32 inputs (mmact_conv2d_nhwc only) are
+ * the fast one-pass alternative: each operand keeps 10 fraction bits, so the
+ * error is up to about 2^-9 * sum_k |x_k w_k|.
+ */
+
+/*
  * Fused single-kernel GEMM + bias + activation:  C = act(A x B + bias).
- *   A     [M, K] ab_dtype (F16 or BF16), row-major
+ *   A     [M, K] ab_dtype (F16, BF16, or F32 in split precision), row-major
  *   B     [K, N] ab_dtype, row-major (N contiguous; not transposed)
  *   bias  [N] fp32, or NULL
  *   C     [M, N] c_dtype (F32, F16 or BF16), row-major; fully overwritten
  *   alpha LeakyReLU slope (ignored by the other activations)
  * Accumulation is fp32 on the tensor cores.  M == 0 or N == 0 enqueues
- * nothing; K == 0 gives C = act(bias).  Requires K % 8 == 0 and N % 8 == 0
- * (16-byte row pitch) else MMACT_ERR_UNSUPPORTED; M, N, K < 2^31.
+ * nothing; K == 0 gives C = act(bias).  16-bit A/B require K % 8 == 0 and
+ * N % 8 == 0 (16-byte row pitch) else MMACT_ERR_UNSUPPORTED; F32 A/B need
+ * only 4-byte alignment (any K, N; C stays 16-byte aligned); TF32 is
+ * MMACT_ERR_UNSUPPORTED here.  M, N, K < 2^31.
  */
 mmact_status mmact_gemm(const void *A, const void *B, const float *bias, void *C,
                         int64_t M, int64_t N, int64_t K,
@@ -130,8 +146,30 @@ mmact_status mmact_gemm_split(const void *A, const void *B, const float *bias, v
                               mmact_act act, float alpha, float *workspace, void *stream);
 
 /*
+ * Fused or two-kernel GEMM, decided per shape at run time (the ops-nn
+ * fused_matmul_relu article's run-time decision between the fused call and
+ * its fallback, matmul into a device temporary then the activation).  The
+ * rule comes from a measured grid of fused against split times on GB300:
+ * the split path is taken for GELU on an output of at most 65536 elements
+ * (one or two tiles: the fused epilogue's few warps are latency-bound on the
+ * activation, the split's activation pass spreads over the GPU), the fused
+ * kernel everywhere else (1.07x to 3.4x faster there).  `workspace`
+ * ([M, N] fp32, 16-byte aligned) may be NULL: then the fused kernel always
+ * runs.  Everything else as mmact_gemm / mmact_gemm_split.
+ */
+mmact_status mmact_gemm_auto(const void *A, const void *B, const float *bias, void *C,
+                             int64_t M, int64_t N, int64_t K,
+                             mmact_dtype ab_dtype, mmact_dtype c_dtype,
+                             mmact_act act, float alpha, float *workspace, void *stream);
+
+/* Which path mmact_gemm_auto takes with a workspace: *split = 1 for the two-kernel
+ * split, 0 for the fused kernel (host only).  MMACT_ERR_INVALID_ARG for bad arguments. */
+mmact_status mmact_gemm_auto_choice(int64_t M, int64_t N, int64_t K, mmact_dtype ab_dtype,
+                                    mmact_dtype c_dtype, mmact_act act, int *split);
+
+/*
  * Fused implicit-GEMM conv2d + bias + activation:  y = act(conv2d(x, w) + bias).
- *   x    [N, C, H, W] in_dtype (F16 or BF16), NCHW
+ *   x    [N, C, H, W] in_dtype (F16, BF16, or F32 in split precision), NCHW
  *   w    [Co, C, kh, kw] in_dtype
  *   bias [Co] fp32, or NULL
  *   y    [N, Co, Ho, Wo] out_dtype (F32, F16 or BF16), NCHW; fully overwritten
@@ -182,6 +220,30 @@ mmact_status mmact_conv2d_split(const void *x, const void *w, const float *bias,
                                 mmact_act act, float alpha, float *workspace, void *stream);
 
 /*
+ * mmact_conv2d or mmact_conv2d_split, decided per geometry at run time as for
+ * mmact_gemm_auto.  The split path is taken for GELU over a contraction
+ * C*kh*kw of at most 288 with Co >= 64, and when the fused kernel would store a 16-bit
+ * output element by element (the output row pitch Ho*Wo*2 is not a
+ * multiple of 16 bytes and neither the tensor-memory nor the vectorised
+ * producer applies), where the split's fp32 intermediate is stored by TMA.
+ * `workspace` ([N, Co, Ho, Wo] fp32) may be NULL: then the fused kernel runs.
+ */
+mmact_status mmact_conv2d_auto(const void *x, const void *w, const float *bias, void *y,
+                               int64_t N, int64_t C, int64_t H, int64_t W,
+                               int64_t Co, int64_t kh, int64_t kw,
+                               const int32_t strides[2], const int32_t pads[4],
+                               const int32_t dilations[2],
+                               mmact_dtype in_dtype, mmact_dtype out_dtype,
+                               mmact_act act, float alpha, float *workspace, void *stream);
+
+/* Which path mmact_conv2d_auto takes with a workspace (*split: 1 split, 0 fused; host only). */
+mmact_status mmact_conv2d_auto_choice(int64_t N, int64_t C, int64_t H, int64_t W, int64_t Co,
+                                      int64_t kh, int64_t kw, const int32_t strides[2],
+                                      const int32_t pads[4], const int32_t dilations[2],
+                                      mmact_dtype in_dtype, mmact_dtype out_dtype, mmact_act act,
+                                      int *split);
+
+/*
  * Largest M*N accepted by mmact_gemm_split_noalloc (fp32 elements of its
  * built-in scratch array: 16 MiB per device).
  */
@@ -227,14 +289,16 @@ mmact_status mmact_gemm_split_noalloc(const void *A, const void *B, const float 
  * Channels-last fused conv2d + bias + activation (the layout-converting
  * member of the fused_matmul_relu article's fusion families applied to the
  * Fused ConvTanh operator):  y = act(conv2d(x, w) + bias).
- *   x    [N, H, W, C] in_dtype (F16, BF16 or F32), channels innermost (NHWC)
+ *   x    [N, H, W, C] in_dtype (F16, BF16, F32 in split precision, or TF32),
+ *        channels innermost (NHWC)
  *   w    [Co, kh, kw, C] in_dtype, channels innermost
  *   bias [Co] fp32, or NULL
  *   y    [N, Ho, Wo, Co] out_dtype (F32, F16 or BF16), NHWC; fully overwritten
- * strides / pads / dilations and Ho, Wo as for mmact_conv2d.  F32 inputs
- * (the Fused ConvTanh article evaluates fp32 cases beside fp16 and bf16) run
- * on the tensor cores as tf32: each operand keeps 10 fraction bits, so
- * |error| <= about 2^-9 * sum_k |x_k w_k| beyond the fp32 accumulation.
+ * strides / pads / dilations and Ho, Wo as for mmact_conv2d.  TF32 inputs
+ * (fp32 storage) run on the tensor cores as tf32 with the operands fed by
+ * TMA: each operand keeps 10 fraction bits, so |error| <= about
+ * 2^-9 * sum_k |x_k w_k| beyond the fp32 accumulation.  F32 inputs run in
+ * split precision on the general gather kernel (fp32 accuracy, slower).
  * Requires C * sizeof(in_dtype) % 16 == 0 and Co % 8 == 0 (16-byte channel
  * rows), else MMACT_ERR_UNSUPPORTED.  N == 0 or Co == 0 enqueues nothing;
  * C == 0 gives y = act(bias).
@@ -251,7 +315,8 @@ mmact_status mmact_conv2d_nhwc(const void *x, const void *w, const float *bias, 
  * mmact_conv2d_nhwc with a residual tensor added before the activation:
  *   y = act(conv2d(x, w) + bias + R), R [N, Ho, Wo, Co] in out_dtype (y's
  *   shape), 16-byte aligned; R == y allowed, other overlaps rejected with
- *   MMACT_ERR_INVALID_ARG.  Everything else as mmact_conv2d_nhwc.
+ *   MMACT_ERR_INVALID_ARG.  F32 (split precision) inputs are
+ *   MMACT_ERR_UNSUPPORTED here.  Everything else as mmact_conv2d_nhwc.
  */
 mmact_status mmact_conv2d_nhwc_residual(const void *x, const void *w, const float *bias, const void *R,
                                         void *y, int64_t N, int64_t C, int64_t H, int64_t W,
@@ -276,7 +341,7 @@ mmact_status mmact_conv2d_out_shape(int64_t H, int64_t W, int64_t kh, int64_t kw
  * would use for this NCHW geometry.  The choice depends only on the shape and
  * dtypes.  Returns a mmact_conv_producer value, or -1 when the arguments are
  * invalid, C == 0, or the problem is too large for the library.
- *   MMACT_CONV_GATHER  per-element im2col gather (any geometry)
+ *   MMACT_CONV_GATHER  per-element im2col gather (any geometry; every F32-input conv)
  *   MMACT_CONV_VECTOR  16-byte chunk loads from global memory + byte picks
  *                      (W % 8 == 0, horizontal stride 1 or 2, filter rows a
  *                      multiple of 16 bytes, output rows TMA-storable)

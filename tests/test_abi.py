@@ -157,8 +157,11 @@ def test_gemm_host_validation(lib):
     assert gemm(lib, M=-1) == E
     assert gemm(lib, K=-8) == E
     assert gemm(lib, N=1 << 31) == E
-    assert gemm(lib, ab=2) == E             # fp32 operands are not a kind::f16 input
+    assert gemm(lib, ab=3) == U             # one-pass tf32 operands: channels-last conv only
+    assert gemm(lib, ab=4) == E
     assert gemm(lib, ab=7) == E
+    assert gemm(lib, ab=2, A=P16 + 2) == U  # fp32 operands (split precision) need 4-byte alignment
+    assert gemm(lib, ab=2, M=0) == OK       # ... and may have any K and N; empty is a no-op
     assert gemm(lib, cd=5) == E
     assert gemm(lib, act=6) == E
     assert gemm(lib, act=-1) == E
@@ -185,7 +188,7 @@ def test_noalloc_checks_arguments_before_its_size_limit(lib):
         return lib.mmact_gemm_split_noalloc(A, P16, None, C, M, N, K, ab, cd, act, ctypes.c_float(0.1), None)
 
     assert na(act=9, M=big_m, N=big_n) == E
-    assert na(ab=2, M=big_m, N=big_n) == E
+    assert na(ab=4, M=big_m, N=big_n) == E
     assert na(A=None, M=big_m, N=big_n) == E
     assert na(M=-1) == E
     assert na(A=P_MIS, M=big_m, N=big_n) == U   # alignment, as for mmact_gemm_split
@@ -224,9 +227,35 @@ def test_conv_host_validation(lib):
     assert conv(pd=(0, -1, 0, 0)) == E
     assert conv(dl=(1, 0)) == E
     assert conv(H=1, pd=(0, 0, 0, 0)) == E   # 3x3 filter on a 1-row input: empty output
-    assert conv(i=2) == E
+    assert conv(i=3) == E                    # one-pass tf32: channels-last only
+    assert conv(i=4) == E
     assert conv(o=3) == E
     assert conv(act=9) == E
     assert conv(x=P_MIS) == U
     assert lib.mmact_conv2d(P16, P16, None, P16, 1, 4, 8, 8, 4, 3, 3, None, i32(0, 0, 0, 0),
                             i32(1, 1), 1, 1, 3, ctypes.c_float(0), None) == E
+
+
+def test_auto_choice_follows_the_measured_rule(lib):
+    import torch
+    bf16, f16, f32 = torch.bfloat16, torch.float16, torch.float32
+    G = mmact.mmact_gemm_auto_choice
+    assert G(64, 64, 64, bf16, bf16, "gelu") == "split"        # GELU on a small output
+    assert G(256, 256, 1024, bf16, bf16, "gelu") == "split"
+    assert G(256, 264, 64, bf16, bf16, "gelu") == "fused"       # more than 64 Ki outputs
+    assert G(8192, 8192, 64, bf16, bf16, "gelu") == "fused"
+    assert G(64, 64, 64, bf16, bf16, "relu") == "fused"         # every other activation: fused
+    assert G(64, 64, 64, bf16, bf16, "tanh") == "fused"
+    assert G(64, 64, 64, f32, f32, "gelu") == "fused"          # fp32 inputs: split precision, fused
+    Cv = mmact.mmact_conv2d_auto_choice
+    # 1x1 stride 2 on 28 x 28: a 14 x 14 output (392-byte rows) would be stored element by element
+    assert Cv(8, 64, 28, 28, 128, 1, 1, (2, 2), (0, 0, 0, 0), (1, 1), f16, f16, "relu") == "split"
+    assert Cv(8, 64, 28, 28, 128, 1, 1, (2, 2), (0, 0, 0, 0), (1, 1), f16, f32, "relu") == "fused"
+    assert Cv(8, 16, 56, 56, 64, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1), f16, f16, "gelu") == "split"
+    assert Cv(32, 16, 32, 32, 32, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1), f16, f16, "gelu") == "fused"
+    assert Cv(8, 64, 56, 56, 128, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1), f16, f16, "tanh") == "fused"
+    out = ctypes.c_int(-5)
+    assert lib.mmact_gemm_auto_choice(-1, 8, 8, 1, 1, 1, ctypes.byref(out)) == mmact.MMACT_ERR_INVALID_ARG
+    assert lib.mmact_gemm_auto_choice(8, 8, 8, 1, 1, 9, ctypes.byref(out)) == mmact.MMACT_ERR_INVALID_ARG
+    assert lib.mmact_gemm_auto_choice(8, 8, 8, 1, 1, 1, None) == mmact.MMACT_ERR_INVALID_ARG
+    assert out.value == -5

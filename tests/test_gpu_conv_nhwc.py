@@ -89,15 +89,16 @@ def test_workload_shapes_channels_last(orc, wl):
 
 
 # ---------------------------------------------------------------- fp32 inputs --
-def run_nhwc_f32(x, w, bias, od, stride, pads, dil, act, alpha=0.0):
-    """fp32 x [N,C,H,W], w [Co,C,kh,kw] (NCHW); returns y as NCHW float64."""
+def run_nhwc_f32(x, w, bias, od, stride, pads, dil, act, alpha=0.0, tf32=False):
+    """fp32 x [N,C,H,W], w [Co,C,kh,kw] (NCHW), computed as tf32 or in split precision;
+    returns y as NCHW float64."""
     Nb, C, H, W = x.shape
     Co, _, kh, kw = w.shape
     Ho, Wo = mmact.mmact_conv2d_out_shape(H, W, kh, kw, stride, pads, dil)
     dx = torch.from_numpy(np.ascontiguousarray(x.transpose(0, 2, 3, 1))).cuda()
     dw = torch.from_numpy(np.ascontiguousarray(w.transpose(0, 2, 3, 1))).cuda()
     y = torch.full((Nb, Ho, Wo, Co), float("nan"), dtype=TORCH[od], device="cuda")
-    mmact.mmact_conv2d_nhwc(dx, dw, fp32_to_device(bias), y, stride, pads, dil, act, alpha)
+    mmact.mmact_conv2d_nhwc(dx, dw, fp32_to_device(bias), y, stride, pads, dil, act, alpha, tf32=tf32)
     assert mmact.mmact_get_last_error() == mmact.MMACT_OK
     return host(y).transpose(0, 3, 1, 2)
 
@@ -118,36 +119,60 @@ F32_CASES = [
 ]
 
 
-@pytest.mark.parametrize("case", F32_CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}x{c[3]}-{c[4]}k{c[5]}{c[6]}s{c[7][0]}{c[7][1]}")
-@pytest.mark.parametrize("act", ["tanh", "relu", "gelu"])
-def test_fp32_inputs_small_geometries(orc, case, act):
+def f32_inputs(case):
     Nb, C, H, W, Co, kh, kw, stride, pads, dil, od = case
     rng = np.random.default_rng(Nb * 100 + C + Co + 7)
+    # full-precision fp32 values (not representable in 16 bits or in tf32)
     x = rng.normal(0, 1, (Nb, C, H, W)).astype(np.float32)
     w = rng.normal(0, (1.0 / (C * kh * kw)) ** 0.5, (Co, C, kh, kw)).astype(np.float32)
     bias = rng.uniform(-0.1, 0.1, Co).astype(np.float32)
+    return x, w, bias
+
+
+CASE_ID = lambda c: f"{c[0]}x{c[1]}x{c[2]}x{c[3]}-{c[4]}k{c[5]}{c[6]}s{c[7][0]}{c[7][1]}"  # noqa: E731
+
+
+@pytest.mark.parametrize("case", F32_CASES, ids=CASE_ID)
+@pytest.mark.parametrize("act", ["tanh", "relu", "gelu"])
+def test_tf32_inputs_small_geometries(orc, case, act):
+    # one-pass tf32: the stated bound plus the tf32 operand-rounding allowance
+    Nb, C, H, W, Co, kh, kw, stride, pads, dil, od = case
+    x, w, bias = f32_inputs(case)
+    y = run_nhwc_f32(x, w, bias, od, stride, pads, dil, act, tf32=True)
+    ref = orc.conv2d(x, w, "f32", bias, stride, pads, dil, act)
+    check(y, ref, od, f"nhwc tf32 {case} {act}", extra=tf32_allowance(orc, x, w, stride, pads, dil))
+
+
+@pytest.mark.parametrize("case", F32_CASES, ids=CASE_ID)
+@pytest.mark.parametrize("act", ["tanh", "relu", "gelu"])
+def test_fp32_split_precision_small_geometries(orc, case, act):
+    # split precision: the stated bound 2e-3 + 2e-3 |y| (+ 1 output ulp), no allowance
+    Nb, C, H, W, Co, kh, kw, stride, pads, dil, od = case
+    x, w, bias = f32_inputs(case)
     y = run_nhwc_f32(x, w, bias, od, stride, pads, dil, act)
     ref = orc.conv2d(x, w, "f32", bias, stride, pads, dil, act)
-    check(y, ref, od, f"nhwc f32 {case} {act}", extra=tf32_allowance(orc, x, w, stride, pads, dil))
+    check(y, ref, od, f"nhwc fp32 split {case} {act}")
 
 
-def test_fp32_inputs_workload_shape(orc):
+@pytest.mark.parametrize("tf32", [True, False], ids=["tf32", "split"])
+def test_fp32_inputs_workload_shape(orc, tf32):
     # the 3x3 stride-1 workload's values, widened to fp32 (exact), sampled
     wl = synth.WORKLOADS["conv3x3_s1p1d1_tanh_8x64x56x56_f16"]
     inp = wl.inputs()
     x = orc.decode(inp["x"], wl.dtype).astype(np.float32)
     w = orc.decode(inp["w"], wl.dtype).astype(np.float32)
-    y = run_nhwc_f32(x, w, inp["bias"], "f32", wl.stride, wl.pads, wl.dilation, wl.act).ravel()
+    y = run_nhwc_f32(x, w, inp["bias"], "f32", wl.stride, wl.pads, wl.dilation, wl.act, tf32=tf32).ravel()
     pts = sample_points(y.size, y.size // 56, 56, 8000, wl.seed + 200)
     ref = orc.conv2d(x, w, "f32", inp["bias"], wl.stride, wl.pads, wl.dilation, wl.act, points=pts)
-    check(y[pts], ref, "f32", "nhwc f32 workload",
-          extra=tf32_allowance(orc, x, w, wl.stride, wl.pads, wl.dilation, points=pts))
+    extra = tf32_allowance(orc, x, w, wl.stride, wl.pads, wl.dilation, points=pts) if tf32 else None
+    check(y[pts], ref, "f32", f"nhwc fp32 workload ({'tf32' if tf32 else 'split'})", extra=extra)
 
 
-def test_fp32_rejects_channel_counts_that_are_not_multiples_of_4():
+@pytest.mark.parametrize("tf32", [True, False], ids=["tf32", "split"])
+def test_fp32_rejects_channel_counts_that_are_not_multiples_of_4(tf32):
     x = torch.zeros((1, 4, 4, 6), dtype=torch.float32, device="cuda")
     w = torch.zeros((8, 3, 3, 6), dtype=torch.float32, device="cuda")
     y = torch.zeros((1, 2, 2, 8), dtype=torch.float32, device="cuda")
     with pytest.raises(mmact.MmactError) as ei:
-        mmact.mmact_conv2d_nhwc(x, w, None, y)
+        mmact.mmact_conv2d_nhwc(x, w, None, y, tf32=tf32)
     assert ei.value.status == mmact.MMACT_ERR_UNSUPPORTED

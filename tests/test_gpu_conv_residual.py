@@ -95,7 +95,7 @@ NHWC_CASES = [
     (1, 64, 8, 8, 64, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1), "f16", "f16"),
     (2, 16, 13, 11, 24, 3, 3, (2, 2), (2, 2, 2, 2), (2, 2), "bf16", "f32"),
     (2, 32, 17, 19, 200, 1, 1, (2, 2), (0, 0, 0, 0), (1, 1), "f16", "bf16"),
-    (1, 36, 10, 12, 40, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1), "f32", "f32"),     # fp32 inputs (tf32)
+    (1, 36, 10, 12, 40, 3, 3, (1, 1), (1, 1, 1, 1), (1, 1), "f32", "f32"),     # fp32 inputs as tf32
 ]
 
 
@@ -119,7 +119,7 @@ def test_nhwc_residual(orc, case):
     R_nhwc = np.ascontiguousarray(R.transpose(0, 2, 3, 1))
     y = torch.full((Nb, Ho, Wo, Co), float("nan"), dtype=TORCH[od], device="cuda")
     mmact.mmact_conv2d_nhwc_residual(dx, dw, fp32_to_device(bias), residual_device(R_nhwc, od), y,
-                                     st, pd, dl, "tanh")
+                                     st, pd, dl, "tanh", tf32=dt == "f32")
     assert mmact.mmact_get_last_error() == mmact.MMACT_OK
     ref = orc.conv2d(x, w, dt, bias, st, pd, dl, "tanh", residual=R, res_dtype=od)
     extra = None

@@ -52,7 +52,9 @@ def test_binding_rejects_bad_tensors():
         mmact.mmact_gemm(A[:, :60].contiguous(), B[:60], None, C)  # K % 8 != 0
     assert ei.value.status == mmact.MMACT_ERR_UNSUPPORTED
     with pytest.raises(TypeError):
-        mmact.mmact_gemm(A.float(), B.float(), None, C)
+        mmact.mmact_gemm(A.int(), B.int(), None, C)                # integer operands
+    with pytest.raises(ValueError):
+        mmact.mmact_gemm(A.float(), B, None, C)                    # fp32 A with bf16 B
     torch.cuda.synchronize()
     assert mmact.mmact_get_last_error() == mmact.MMACT_OK
 
