@@ -103,23 +103,67 @@ CUtensorMapDataType tmap_type(mmact_dtype d)
 // the byte strides of dims 1..rank-1, with a 128-byte swizzle (or none).
 // `estrides` (optional) are TMA traversal strides per dimension: a box of
 // box[i] elements along dimension i then delivers ceil(box[i] / estrides[i]).
+//
+// A tensor map is a pure function of these arguments (it holds the address,
+// not the memory), so encoded maps are kept in a small per-thread cache keyed
+// by every argument: a repeated call with the same tensors, shapes and dtypes
+// copies 128 bytes instead of encoding again, and a stale entry cannot exist.
+struct TmapKey {
+    int32_t dt, rank, swizzle, pad;
+    const void *ptr;
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], es[5];
+};
+struct TmapEntry {
+    CUtensorMap map;
+    TmapKey key;
+    bool valid;
+};
+constexpr int TMAP_CACHE_ENTRIES = 256;      // direct-mapped, per host thread
+thread_local TmapEntry t_tmap_cache[TMAP_CACHE_ENTRIES];
+std::atomic<uint64_t> g_tmap_hits{0}, g_tmap_encodes{0};
+
+uint64_t tmap_hash(const TmapKey &k)
+{
+    // FNV-1a over the key's bytes (the key is zero-filled, so padding is defined)
+    const unsigned char *b = reinterpret_cast<const unsigned char *>(&k);
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < sizeof(k); ++i) h = (h ^ b[i]) * 1099511628211ull;
+    return h;
+}
+
 bool encode(CUtensorMap *m, mmact_dtype dt, int rank, const void *ptr, const uint64_t *dims,
             const uint64_t *strides_bytes, const uint32_t *box, bool swizzle = true,
             const uint32_t *estrides = nullptr)
 {
-    cuuint64_t gd[5], gs[4];
-    cuuint32_t bx[5], es[5];
+    TmapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.dt = (int32_t)tmap_type(dt);
+    k.rank = rank;
+    k.swizzle = swizzle ? 1 : 0;
+    k.ptr = ptr;
     for (int i = 0; i < rank; ++i) {
-        gd[i] = dims[i];
-        bx[i] = box[i];
-        es[i] = estrides ? estrides[i] : 1;
+        k.gd[i] = dims[i];
+        k.bx[i] = box[i];
+        k.es[i] = estrides ? estrides[i] : 1;
     }
-    for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
-    CUresult r = g_encode(m, tmap_type(dt), (cuuint32_t)rank, const_cast<void *>(ptr), gd, gs, bx, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+    for (int i = 0; i + 1 < rank; ++i) k.gs[i] = strides_bytes[i];
+    TmapEntry &e = t_tmap_cache[tmap_hash(k) % TMAP_CACHE_ENTRIES];
+    if (e.valid && std::memcmp(&e.key, &k, sizeof(k)) == 0) {
+        *m = e.map;
+        g_tmap_hits.fetch_add(1, std::memory_order_relaxed);
+        return true;
+    }
+    CUresult r = g_encode(m, (CUtensorMapDataType)k.dt, (cuuint32_t)rank, const_cast<void *>(ptr), k.gd, k.gs,
+                          k.bx, k.es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) return false;
+    g_tmap_encodes.fetch_add(1, std::memory_order_relaxed);
+    e.key = k;
+    e.map = *m;
+    e.valid = true;
+    return true;
 }
 
 bool valid_act(mmact_act a) { return a >= MMACT_ACT_NONE && a <= MMACT_ACT_GELU; }
@@ -1179,6 +1223,13 @@ MMACT_EXPORT mmact_status mmact_set_conv_tmem(int mode)
 {
     if (mode != 0 && mode != 1) return MMACT_ERR_INVALID_ARG;
     g_conv_tmem.store(mode);
+    return MMACT_OK;
+}
+
+MMACT_EXPORT mmact_status mmact_tensor_map_cache_stats(uint64_t *hits, uint64_t *encodes)
+{
+    if (hits != nullptr) *hits = g_tmap_hits.load();
+    if (encodes != nullptr) *encodes = g_tmap_encodes.load();
     return MMACT_OK;
 }
 

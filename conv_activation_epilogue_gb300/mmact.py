@@ -34,7 +34,7 @@ SYMBOLS = [
     "mmact_selftest_wait_timeout", "mmact_set_gemm_tile_n", "mmact_set_gemm_split_k",
     "mmact_gemm_split_k_choice", "mmact_set_gemm_pair", "mmact_gemm_kernel_choice", "mmact_set_conv_tmem",
     "mmact_gemm_auto", "mmact_gemm_auto_choice", "mmact_conv2d_auto", "mmact_conv2d_auto_choice",
-    "mmact_status_string", "mmact_version",
+    "mmact_tensor_map_cache_stats", "mmact_status_string", "mmact_version",
 ]
 
 
@@ -95,6 +95,8 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     L.mmact_set_conv_tmem.argtypes = [ci]
     L.mmact_gemm_kernel_choice.argtypes = [i64, i64, i64, ci, ctypes.POINTER(ci)]
     L.mmact_gemm_split_k_choice.argtypes = [i64, i64, i64, ctypes.POINTER(ci)]
+    L.mmact_tensor_map_cache_stats.argtypes = [ctypes.POINTER(u64), ctypes.POINTER(u64)]
+    L.mmact_tensor_map_cache_stats.restype = ci
     L.mmact_status_string.argtypes = [ci]
     L.mmact_status_string.restype = ctypes.c_char_p
     L.mmact_version.argtypes = []
@@ -117,8 +119,16 @@ def _check(status: int, where: str) -> None:
         raise MmactError(status, where)
 
 
+# the current stream's raw handle without building a torch.cuda.Stream object
+# (a few microseconds per call on small launches); torch's public route otherwise
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_CUR_DEVICE = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream_handle(stream) -> int | None:
     if stream is None:
+        if _RAW_STREAM is not None and _CUR_DEVICE is not None:
+            return _RAW_STREAM(_CUR_DEVICE()) or None
         stream = torch.cuda.current_stream()
     if isinstance(stream, int):
         return stream or None
@@ -415,6 +425,13 @@ def mmact_set_gemm_pair(mode: int) -> None:
 def mmact_set_conv_tmem(mode: int) -> None:
     """NCHW conv with the im2col operand in tensor memory: 0 where it applies (default); 1 never."""
     _check(load().mmact_set_conv_tmem(int(mode)), "mmact_set_conv_tmem")
+
+
+def mmact_tensor_map_cache_stats() -> tuple[int, int]:
+    """(hits, encodes) of the library's host-side tensor-map cache, process-wide."""
+    h, e = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check(load().mmact_tensor_map_cache_stats(ctypes.byref(h), ctypes.byref(e)), "mmact_tensor_map_cache_stats")
+    return int(h.value), int(e.value)
 
 
 GEMM_KERNELS = {0: "none", 1: "persistent", 2: "pair", 3: "split_k"}

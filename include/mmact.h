@@ -433,6 +433,17 @@ mmact_status mmact_set_gemm_pair(int mode);
  */
 mmact_status mmact_set_conv_tmem(int mode);
 
+/*
+ * Tensor-map cache counters (diagnostic; no counterpart in the pages).  Every
+ * call encodes up to four TMA tensor maps on the host; an encoded map depends
+ * only on its address, shape, strides, box and dtype, so the library keeps the
+ * last 256 per host thread, keyed by all of them, and a call that repeats an
+ * earlier call's tensors and shapes copies them instead of encoding again.
+ * Writes the process-wide number of cache hits and of encodes so far (either
+ * pointer may be null).  Never fails.
+ */
+mmact_status mmact_tensor_map_cache_stats(uint64_t *hits, uint64_t *encodes);
+
 /* The GEMM kernels an mmact_gemm-family call can run. */
 typedef enum {
     MMACT_GEMM_KERNEL_NONE = 0,        /* empty output or K = 0: the bias/activation fill only */
