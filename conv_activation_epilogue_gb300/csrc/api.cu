@@ -32,6 +32,7 @@ std::atomic<int> g_tile_n{0};
 std::atomic<int> g_split_k{0};   // 0: chosen per shape; 1: never; 2 or 4: whenever legal
 std::atomic<int> g_pair{0};      // CTA-pair GEMM kernel: 0 chosen per shape; 1 never; 2 always
 std::atomic<int> g_conv_tmem{0}; // NCHW conv, im2col operand in TMEM: 0 when supported; 1 never
+std::atomic<int> g_l2_policy{1}; // CTA-pair GEMM: 1 A evict-last, C evict-first (default); 0 no cache hints
 
 constexpr int MAX_DEVICES = 64;
 struct DeviceInfo {
@@ -228,17 +229,17 @@ int choose_split_k(const DeviceInfo &dev, int64_t tiles_m, int64_t N, int64_t nu
 // persistent one: each wave of either does 128 x 256 outputs per SM, and a
 // pair wave was measured faster (bf16 on GB300: 8192^3 639 -> 577 us,
 // 8192x8192x4096 326 -> 282, 4096^3 94.6 -> 81.8, 16384x4096x1024
-// 89.8 -> 82.8).  Not with a residual over 16 or fewer K blocks: there the
-// epilogue (which reads the residual) outlasts the main loop, and a pair
-// releases its accumulator only when both CTAs' epilogues are done
-// (16384x4096x1024 with residual: 103 us persistent, 116 us pair).
+// 89.8 -> 82.8).  With a residual too, since the pair kernel stages the
+// residual tiles by TMA one epilogue unit ahead (16384x4096x1024 with
+// residual: 98.4 us on the pair, 103.9 us persistent).
 bool choose_pair(const DeviceInfo &dev, int64_t M, int64_t N, int64_t num_kb, bool has_res)
 {
+    (void)num_kb;
+    (void)has_res;
     const int mode = g_pair.load();
     if (mode == 1 || dev.pair_clusters <= 0) return false;
     if (mode == 2) return true;
     if (g_tile_n.load() != 0) return false;
-    if (has_res && num_kb <= 16) return false;
     const int64_t tiles_m = (M + 127) / 128;
     if (choose_tile_n(tiles_m, N, dev.sm_count) != 256) return false;
     const int64_t tiles_n = (N + 255) / 256;
@@ -281,7 +282,12 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
     a.tiles_n = tiles_n;
     a.num_tiles = tiles_m * tiles_n;
     a.num_kb = (int)((K + 63) / 64);
-    a.group_m = 16;
+    // M blocks per raster group: 16 of 128 rows; on CTA pairs 8 of 256 rows (a wave
+    // of 76 pair tiles then spans ~8 x 9.5 blocks, near the least A + B read per
+    // wave, and with the evict-last hint the group's A rows stay in L2 across its
+    // waves; measured on GB300 at 6144^3: 406 MB of DRAM traffic per launch, 1.9x
+    // the algorithmic bytes, and 4096^3 88 -> 82 us)
+    a.group_m = pair ? 8 : 16;
     a.ab_bf16 = ab == MMACT_BF16 ? 1 : 0;
     a.act = (int)act;
     a.alpha = alpha;
@@ -289,6 +295,7 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
     a.res = res;
     a.status = dev->status;
     a.wait_ns = g_wait_ns.load();
+    a.l2_policy = g_l2_policy.load();
     L.tile_n = bn;
     L.out = out_kind(cd);
     L.grid = (int)std::min<int64_t>(a.num_tiles, dev->sm_count);
@@ -319,6 +326,7 @@ mmact_status gemm_enqueue(const void *A, const void *B, const float *bias, void 
         const uint32_t bT[2] = {32, 32};
         if (!encode(&L.tmCt, cd, 2, C, dC, sC, bT, false)) return MMACT_ERR_CUDA;
     }
+    if (pair && res != nullptr && !encode(&L.tmR, cd, 2, res, dC, sC, bC)) return MMACT_ERR_CUDA;
     const cudaError_t e = split != 0 ? launch_gemm_splitk(L, stream)
                           : pair       ? launch_gemm_pair(L, stream)
                                        : launch_gemm(L, stream);
@@ -1223,6 +1231,13 @@ MMACT_EXPORT mmact_status mmact_set_conv_tmem(int mode)
 {
     if (mode != 0 && mode != 1) return MMACT_ERR_INVALID_ARG;
     g_conv_tmem.store(mode);
+    return MMACT_OK;
+}
+
+MMACT_EXPORT mmact_status mmact_set_gemm_l2_policy(int mode)
+{
+    if (mode != 0 && mode != 1) return MMACT_ERR_INVALID_ARG;
+    g_l2_policy.store(mode);
     return MMACT_OK;
 }
 

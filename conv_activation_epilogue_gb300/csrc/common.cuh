@@ -349,11 +349,40 @@ __device__ __forceinline__ void add_residual(const void *res, int nvalid, float 
     }
 }
 
+// Adds this lane's residual row segment staged in shared memory by a TMA load
+// through the output's tensor map (128-byte rows, 16-byte chunk c of row r at
+// chunk c ^ (r & 7)): the 8 chunks of `row`, swizzled by `sw`.
+template <int OUT, int COLS>
+__device__ __forceinline__ void add_residual_smem(uint32_t row, uint32_t sw, float (&v)[COLS])
+{
+    constexpr int PER = OUT == OUT_F32 ? 4 : 8;
+    static_assert(COLS == 8 * PER, "one 128-byte row segment");
+    uint4 u[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) u[c] = ptx::ld_shared_v4(row + (((uint32_t)c ^ sw) << 4));
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if constexpr (OUT == OUT_F32) {
+                v[4 * c + e] += __uint_as_float(w[e]);
+            } else {
+                const float2 f = unpack2<OUT>(w[e]);
+                v[8 * c + 2 * e] += f.x;
+                v[8 * c + 2 * e + 1] += f.y;
+            }
+        }
+    }
+}
+
 // One epilogue unit: 32 rows (this warp's TMEM lane quarter) x one 128-byte
 // output row segment (32 fp32 or 64 16-bit columns).  Loads the fp32
 // accumulators from TMEM, adds the fp32 bias (per column from global memory
 // `bias_col[0..nvalid)`, zero beyond it or when null; or the per-row `brow`),
-// adds the lane's residual row segment when `res` is not null, applies the
+// adds the lane's residual row segment when `res` is not null (with RSMEM: the
+// segment already staged in `buf` at this lane's row, which the output then
+// overwrites in place), applies the
 // activation in fp32, converts, and writes the row into a
 // 32 x 128 B shared buffer in the 128-byte swizzled order a TMA store expects
 // (16-byte chunk c of row r lands at chunk c ^ (r & 7)).
@@ -361,11 +390,13 @@ __device__ __forceinline__ void add_residual(const void *res, int nvalid, float 
 // NCOL = 32 with a 16-bit output is the narrow tail unit of a 224-wide tile:
 // 64-byte rows, written densely without swizzle (its TMA store uses an
 // unswizzled map).
-template <int OUT, int ACT, bool BIAS_ROW, int NCOL, bool RES>
+template <int OUT, int ACT, bool BIAS_ROW, int NCOL, bool RES, bool RSMEM = false>
 __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, int nvalid,
                                          float brow, float alpha, uint32_t buf, int lane,
                                          const void *res)
 {
+    static_assert(!RSMEM || (RES && !BIAS_ROW && NCOL * (OUT == OUT_F32 ? 4 : 2) == 128),
+                  "a staged residual is a whole 128-byte row segment with a per-column bias");
     constexpr int COLS = NCOL;
     constexpr bool WIDE = COLS == 64;                  // two TMEM loads per unit
     uint32_t r0[32];
@@ -394,7 +425,9 @@ __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, 
     // loads issued together before the TMEM wait.  With a per-row bias (NCHW
     // conv) bc[] folds to one register, so the residual is read chunk by
     // chunk in the packing loops instead (from L1: the caller prefetches).
-    if constexpr (RES && !BIAS_ROW) {
+    if constexpr (RSMEM) {
+        add_residual_smem<OUT, COLS>(buf + (uint32_t)lane * 128u, (uint32_t)(lane & 7), bc);
+    } else if constexpr (RES && !BIAS_ROW) {
         add_residual<OUT, COLS>(res, nvalid, bc);
         __syncwarp();                                  // converge before the warp-collective wait
     }
@@ -455,29 +488,29 @@ __device__ __forceinline__ void epi_unit(uint32_t taddr, const float *bias_col, 
     }
 }
 
-template <int OUT, bool BIAS_ROW, int NCOL, bool RES>
+template <int OUT, bool BIAS_ROW, int NCOL, bool RES, bool RSMEM = false>
 __device__ __forceinline__ void epi_unit_act(int act, uint32_t taddr, const float *bias_col, int nvalid,
                                              float brow, float alpha, uint32_t buf, int lane,
                                              const void *res)
 {
     switch (act) {
     case ACT_RELU:
-        epi_unit<OUT, ACT_RELU, BIAS_ROW, NCOL, RES>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+        epi_unit<OUT, ACT_RELU, BIAS_ROW, NCOL, RES, RSMEM>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     case ACT_LEAKY:
-        epi_unit<OUT, ACT_LEAKY, BIAS_ROW, NCOL, RES>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+        epi_unit<OUT, ACT_LEAKY, BIAS_ROW, NCOL, RES, RSMEM>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     case ACT_TANH:
-        epi_unit<OUT, ACT_TANH, BIAS_ROW, NCOL, RES>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+        epi_unit<OUT, ACT_TANH, BIAS_ROW, NCOL, RES, RSMEM>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     case ACT_SIGMOID:
-        epi_unit<OUT, ACT_SIGMOID, BIAS_ROW, NCOL, RES>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+        epi_unit<OUT, ACT_SIGMOID, BIAS_ROW, NCOL, RES, RSMEM>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     case ACT_GELU:
-        epi_unit<OUT, ACT_GELU, BIAS_ROW, NCOL, RES>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+        epi_unit<OUT, ACT_GELU, BIAS_ROW, NCOL, RES, RSMEM>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     default:
-        epi_unit<OUT, ACT_NONE, BIAS_ROW, NCOL, RES>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+        epi_unit<OUT, ACT_NONE, BIAS_ROW, NCOL, RES, RSMEM>(taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
         break;
     }
 }
@@ -496,6 +529,15 @@ __device__ __forceinline__ void epi_unit_dispatch(int act, uint32_t taddr, const
         epi_unit_act<OUT, BIAS_ROW, NCOL, true>(act, taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
     else
         epi_unit_act<OUT, BIAS_ROW, NCOL, false>(act, taddr, bias_col, nvalid, brow, alpha, buf, lane, res);
+}
+
+// The same unit with the residual already staged in `buf` (warp-uniform
+// choice between the two by the caller).
+template <int OUT, int NCOL = (OUT == OUT_F32 ? 32 : 64)>
+__device__ __forceinline__ void epi_unit_dispatch_rsmem(int act, uint32_t taddr, const float *bias_col,
+                                                        int nvalid, float alpha, uint32_t buf, int lane)
+{
+    epi_unit_act<OUT, false, NCOL, true, true>(act, taddr, bias_col, nvalid, 0.0f, alpha, buf, lane, nullptr);
 }
 
 }  // namespace mmact

@@ -44,7 +44,8 @@ struct PairCfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int NUM_BARS = 2 * STAGES + 5 + 8;           // + residual loads: 4 warps x 2 buffers
+    static constexpr int OFF_RBAR = OFF_BAR + (2 * STAGES + 5) * 8;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;       // [0] tmem base, [1] abort
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -66,12 +67,12 @@ __device__ __forceinline__ void pair_tile(int t, const GemmArgs &p, int &mb, int
 template <int OUT>
 __global__ void __launch_bounds__(192, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const GemmArgs p)
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
+                     const GemmArgs p)
 {
     using Cfg = PairCfg;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int COLS = OUT == OUT_F32 ? 32 : 64;
-    constexpr int ESZ = OUT == OUT_F32 ? 4 : 2;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t base = ptx::smem_addr(smem);
@@ -111,6 +112,7 @@ __global__ void __launch_bounds__(192, 1)
                 ptx::mbar_init(pp.tempty0 + 8 * a, 8);    // 4 epilogue warps x 2 CTAs
             }
             ptx::mbar_init(pp.drain, 1);
+            for (int b = 0; b < 8; ++b) ptx::mbar_init(base + Cfg::OFF_RBAR + 8 * b, 1);
             misc[1] = 0;
             ptx::fence_mbar_init();
         }
@@ -142,6 +144,10 @@ __global__ void __launch_bounds__(192, 1)
             // -------------------------------------------------------- producer --
             uint32_t stage = 0, phase = 0;
             bool ok = true;
+            // A strips are reused by every wave of a raster group (8 M blocks of 256 rows);
+            // a B strip only by the tiles of one wave.  With l2_policy the A loads carry
+            // the evict-last policy so that the group's A rows stay in L2 across its waves.
+            const uint64_t pol_a = ptx::createpolicy_evict_last();
             for (int t = pair; t < p.num_tiles && ok; t += npairs) {
                 int mb, nb;
                 pair_tile(t, p, mb, nb);
@@ -150,8 +156,12 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t fb = pp.full0 + 8 * stage;
                     if (leader) ptx::mbar_arrive_expect_tx(fb, 2u * Cfg::STAGE_BYTES);
                     const uint32_t fb_leader = ptx::mapa(fb, 0);
-                    ptx::tma_load_2d_pair(sA + stage * Cfg::A_BYTES, &tmA, fb_leader, kb * 64,
-                                          mb * 256 + (int)rank * 128);
+                    if (p.l2_policy != 0)
+                        ptx::tma_load_2d_pair_hint(sA + stage * Cfg::A_BYTES, &tmA, fb_leader, kb * 64,
+                                                   mb * 256 + (int)rank * 128, pol_a);
+                    else
+                        ptx::tma_load_2d_pair(sA + stage * Cfg::A_BYTES, &tmA, fb_leader, kb * 64,
+                                              mb * 256 + (int)rank * 128);
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
                         ptx::tma_load_2d_pair(sB + stage * Cfg::B_BYTES + c * 8192, &tmB, fb_leader,
@@ -202,6 +212,30 @@ __global__ void __launch_bounds__(192, 1)
         const int q = warp & 3;
         const uint32_t my_buf = base + Cfg::OFF_EPI + (uint32_t)q * 8192u;
         const uint32_t tempty_leader = ptx::mapa(pp.tempty0, 0);
+        const uint64_t pol_c = ptx::createpolicy_evict_first();   // C is never read back here
+        // Residual: each unit's R tile [32 rows][128 B] is loaded by TMA (the output's
+        // tensor map layout, on R) into the staging buffer the unit's output will use,
+        // one unit ahead: the load for unit i+1 is issued, into the other buffer, once
+        // every earlier store has read its buffer, and unit i waits only for its own.
+        // Each lane reads its R row segment before overwriting it with its output, and
+        // every element of R is loaded before the store of the same element of C (R
+        // may be C itself).
+        const bool has_res = p.res != nullptr;
+        const uint32_t rbar0 = base + Cfg::OFF_RBAR + (uint32_t)q * 16u;
+        uint32_t rphase = 0, rpending = 0;
+        constexpr int NU = 256 / COLS;                      // units per tile for this warp
+        auto load_r = [&](int t_, int u_, uint32_t b) {     // lane 0 only
+            int mb_, nb_;
+            pair_tile(t_, p, mb_, nb_);
+            const uint32_t bar = rbar0 + 8u * b;
+            ptx::mbar_arrive_expect_tx(bar, 4096u);
+            ptx::tma_load_2d(my_buf + b * 4096u, &tmR, bar, nb_ * 256 + u_ * COLS, mb_ * 256 + (int)rank * 128 + q * 32);
+            rpending |= 1u << b;
+        };
+        if (has_res && pair < p.num_tiles && lane == 0) {
+            ptx::prefetch_tensormap(&tmR);
+            load_r(pair, 0, 0u);                            // units == 0: buffer 0
+        }
         uint32_t acc = 0, acc_phase = 0, units = 0;
         bool ok = true;
         for (int t = pair; t < p.num_tiles; t += npairs) {
@@ -212,23 +246,38 @@ __global__ void __launch_bounds__(192, 1)
             ptx::tc_fence_after();
             const uint32_t tbase = pp.tmem + ((uint32_t)(q * 32) << 16) + acc * Cfg::ACC_STRIDE;
             const int row0 = mb * 256 + (int)rank * 128 + q * 32;
-            const int grow = row0 + lane;
 #pragma unroll 1
-            for (int u = 0; u < 256 / COLS; ++u) {
-                const uint32_t buf = my_buf + (units++ & 1u) * 4096u;
-                if (lane == 0) ptx::bulk_wait_read<1>();
-                __syncwarp();
+            for (int u = 0; u < NU; ++u) {
+                const uint32_t cur = units++ & 1u;
+                const uint32_t buf = my_buf + cur * 4096u;
                 const int col0 = n0 + u * COLS;
-                const void *rrow = (p.res != nullptr && grow < p.M)
-                                       ? static_cast<const char *>(p.res) + ((int64_t)grow * p.N + col0) * ESZ
-                                       : nullptr;
-                epi_unit_dispatch<OUT, false>(p.act, tbase + u * COLS,
-                                              p.bias != nullptr ? p.bias + col0 : nullptr, p.N - col0,
-                                              0.0f, p.alpha, buf, lane, rrow, p.res != nullptr);
+                if (has_res) {
+                    if (lane == 0) {
+                        // the next unit's R into the other buffer, once every store has read it
+                        const int tn = u + 1 < NU ? t : t + npairs;
+                        if (tn < p.num_tiles) {
+                            ptx::bulk_wait_read<0>();
+                            load_r(tn, u + 1 < NU ? u + 1 : 0, cur ^ 1u);
+                        }
+                    }
+                    __syncwarp();
+                    if (!warp_epi_wait(pp, rbar0 + 8u * cur, (rphase >> cur) & 1u)) { ok = false; break; }
+                    rphase ^= 1u << cur;
+                    rpending &= ~(1u << cur);
+                    epi_unit_dispatch_rsmem<OUT>(p.act, tbase + u * COLS, p.bias != nullptr ? p.bias + col0 : nullptr,
+                                                 p.N - col0, p.alpha, buf, lane);
+                } else {
+                    if (lane == 0) ptx::bulk_wait_read<1>();
+                    __syncwarp();
+                    epi_unit_dispatch<OUT, false>(p.act, tbase + u * COLS,
+                                                  p.bias != nullptr ? p.bias + col0 : nullptr, p.N - col0,
+                                                  0.0f, p.alpha, buf, lane);
+                }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && row0 < p.M && col0 < p.N) {
-                    ptx::tma_store_2d(&tmC, buf, col0, row0);
+                    if (p.l2_policy != 0) ptx::tma_store_2d_hint(&tmC, buf, col0, row0, pol_c);
+                    else ptx::tma_store_2d(&tmC, buf, col0, row0);
                     ptx::bulk_commit();
                 }
             }
@@ -242,7 +291,13 @@ __global__ void __launch_bounds__(192, 1)
             if (acc == 0) acc_phase ^= 1u;
         }
         if (!ok) pipe_fail(pp);
-        if (lane == 0) ptx::bulk_wait<0>();
+        if (lane == 0) {
+            // a residual load still in flight (after a failed wait) lands before exit
+            for (uint32_t b = 0; b < 2; ++b)
+                if (rpending & (1u << b))
+                    ptx::mbar_wait_bounded(rbar0 + 8u * b, (rphase >> b) & 1u, DRAIN_NS, nullptr);
+            ptx::bulk_wait<0>();
+        }
         __syncwarp();
     }
 
@@ -276,7 +331,7 @@ static cudaError_t launch_pair_t(const GemmLaunch &L, cudaStream_t stream)
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OUT>, L.tmA, L.tmB, L.tmC, L.args);
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<OUT>, L.tmA, L.tmB, L.tmC, L.tmR, L.args);
 }
 
 cudaError_t setup_pair_kernels()

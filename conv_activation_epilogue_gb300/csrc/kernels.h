@@ -20,10 +20,12 @@ struct GemmArgs {
     const void *res;     // residual [M, N] in the output dtype, or null
     unsigned int *status;
     unsigned long long wait_ns;
+    int l2_policy;       // CTA-pair kernel: 0 no hints; 1 B and C evict-first (A strips stay in L2)
 };
 
 struct GemmLaunch {
     CUtensorMap tmA, tmB, tmC, tmCt;   // tmCt: 32-column tail store map (224-wide tiles)
+    CUtensorMap tmR;                   // residual, laid out as tmC (CTA-pair kernel; when res != null)
     GemmArgs args;
     int tile_n;          // 64, 128, 192, 224 or 256
     int out;             // OUT_*
@@ -169,6 +171,7 @@ int splitk_max_clusters(int S);
 cudaError_t setup_pair_kernels();
 cudaError_t launch_gemm_pair(const GemmLaunch &L, cudaStream_t stream);
 int pair_max_clusters();
+
 cudaError_t launch_conv(const ConvLaunch &L, cudaStream_t stream);
 // out[i] = act(ws[i]) for i < count (ws fp32, out of dtype `out`).
 cudaError_t launch_act(const float *ws, void *out, int64_t count, int out_kind, int act,

@@ -34,7 +34,7 @@ SYMBOLS = [
     "mmact_selftest_wait_timeout", "mmact_set_gemm_tile_n", "mmact_set_gemm_split_k",
     "mmact_gemm_split_k_choice", "mmact_set_gemm_pair", "mmact_gemm_kernel_choice", "mmact_set_conv_tmem",
     "mmact_gemm_auto", "mmact_gemm_auto_choice", "mmact_conv2d_auto", "mmact_conv2d_auto_choice",
-    "mmact_tensor_map_cache_stats", "mmact_status_string", "mmact_version",
+    "mmact_set_gemm_l2_policy", "mmact_tensor_map_cache_stats", "mmact_status_string", "mmact_version",
 ]
 
 
@@ -93,6 +93,8 @@ def load(path: str = LIBRARY) -> ctypes.CDLL:
     L.mmact_set_gemm_split_k.argtypes = [ci]
     L.mmact_set_gemm_pair.argtypes = [ci]
     L.mmact_set_conv_tmem.argtypes = [ci]
+    L.mmact_set_gemm_l2_policy.argtypes = [ci]
+    L.mmact_set_gemm_l2_policy.restype = ci
     L.mmact_gemm_kernel_choice.argtypes = [i64, i64, i64, ci, ctypes.POINTER(ci)]
     L.mmact_gemm_split_k_choice.argtypes = [i64, i64, i64, ctypes.POINTER(ci)]
     L.mmact_tensor_map_cache_stats.argtypes = [ctypes.POINTER(u64), ctypes.POINTER(u64)]
@@ -425,6 +427,11 @@ def mmact_set_gemm_pair(mode: int) -> None:
 def mmact_set_conv_tmem(mode: int) -> None:
     """NCHW conv with the im2col operand in tensor memory: 0 where it applies (default); 1 never."""
     _check(load().mmact_set_conv_tmem(int(mode)), "mmact_set_conv_tmem")
+
+
+def mmact_set_gemm_l2_policy(mode: int) -> None:
+    """CTA-pair GEMM: 1 A evict-last and C evict-first in L2 (default); 0 no cache hints."""
+    _check(load().mmact_set_gemm_l2_policy(int(mode)), "mmact_set_gemm_l2_policy")
 
 
 def mmact_tensor_map_cache_stats() -> tuple[int, int]:

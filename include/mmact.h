@@ -434,6 +434,18 @@ mmact_status mmact_set_gemm_pair(int mode);
 mmact_status mmact_set_conv_tmem(int mode);
 
 /*
+ * L2 cache policy of the CTA-pair GEMM kernel (diagnostic; no counterpart in
+ * the pages).  The kernel rasters its 256 x 256 tiles in groups of 8 M
+ * blocks: every wave of tiles in a group reads the same A rows, while a B
+ * column strip is read by the tiles of one wave only.  mode 1 (the default)
+ * loads A with the L2 evict-last policy, so that the group's A rows stay in
+ * L2 across its waves, and stores C with evict-first (C is not read back);
+ * mode 0 issues the same copies without cache hints.  Results are identical.
+ * Returns MMACT_ERR_INVALID_ARG for other values.
+ */
+mmact_status mmact_set_gemm_l2_policy(int mode);
+
+/*
  * Tensor-map cache counters (diagnostic; no counterpart in the pages).  Every
  * call encodes up to four TMA tensor maps on the host; an encoded map depends
  * only on its address, shape, strides, box and dtype, so the library keeps the

@@ -64,12 +64,16 @@ def lib_free_shape(wl):
 
 
 def test_tensor_capacity_fractions():
-    rec = bench.tensor_capacity(1872.0, 152, 1537.0, 2070.0)
+    # burst against the capacity at the maximum clock, sustained against the sampled clock
+    rec = bench.tensor_capacity(1872.0, 152, 1537.0, 2070.0, sustained_tflops=1700.0)
+    cap_max = 152 * 8192 * 2070e6 / 1e12
     cap = 152 * 8192 * 1537e6 / 1e12
+    assert rec["peak_tflops_at_max_clock"] == pytest.approx(cap_max)
+    assert rec["frac_at_max_clock"] == pytest.approx(1872.0 / cap_max)
     assert rec["peak_tflops_at_sampled_clock"] == pytest.approx(cap)
-    assert rec["frac_at_sampled_clock"] == pytest.approx(1872.0 / cap)
-    assert rec["peak_tflops_at_max_clock"] == pytest.approx(152 * 8192 * 2070e6 / 1e12)
+    assert rec["sustained_frac_at_sampled_clock"] == pytest.approx(1700.0 / cap)
     assert rec["frac_of_nominal"] == pytest.approx(1872.0 / 2250.0)
+    assert "sustained_frac_at_sampled_clock" not in bench.tensor_capacity(1872.0, 152, 1537.0, 2070.0)
 
 
 def test_roofline_bound_follows_the_ridge_point():

@@ -122,7 +122,7 @@ def test_automatic_choice():
         assert mmact.mmact_gemm_kernel_choice(128, 8192, 8192) == "split_k"
         assert mmact.mmact_gemm_kernel_choice(0, 64, 64) == "none"
         assert mmact.mmact_gemm_kernel_choice(8192, 8192, 8192, residual=True) == "pair"
-        assert mmact.mmact_gemm_kernel_choice(16384, 4096, 1024, residual=True) == "persistent"
+        assert mmact.mmact_gemm_kernel_choice(16384, 4096, 1024, residual=True) == "pair"   # TMA-staged residual
         mmact.mmact_set_gemm_tile_n(256)
         assert mmact.mmact_gemm_kernel_choice(8192, 8192, 8192) == "persistent"  # a fixed tile width
         mmact.mmact_set_gemm_tile_n(0)
@@ -132,3 +132,23 @@ def test_automatic_choice():
         mmact.mmact_set_gemm_tile_n(0)
         mmact.mmact_set_gemm_pair(2)
         mmact.mmact_set_gemm_split_k(1)
+
+
+@pytest.mark.parametrize("shape", [(1024, 1024, 512), (700, 1000, 256)], ids=lambda s: "x".join(map(str, s)))
+def test_l2_policy_changes_no_value(orc, shape):
+    """The L2 eviction hints rank lines for eviction only: the output with and
+    without them is bit-identical and matches the oracle."""
+    M, N, K = shape
+    rng = np.random.default_rng(M + N)
+    A = rand_codes(rng, (M, K), "bf16")
+    B = rand_codes(rng, (K, N), "bf16")
+    bias = rng.uniform(-1, 1, N).astype(np.float32)
+    try:
+        mmact.mmact_set_gemm_l2_policy(0)
+        plain = host(run(A, B, bias, "bf16", "bf16", "leaky_relu", 0.2))
+        mmact.mmact_set_gemm_l2_policy(1)
+        hinted = host(run(A, B, bias, "bf16", "bf16", "leaky_relu", 0.2))
+    finally:
+        mmact.mmact_set_gemm_l2_policy(1)
+    assert np.array_equal(plain, hinted)
+    check(hinted, orc.gemm(A, B, "bf16", bias, "leaky_relu", 0.2), "bf16", f"pair with L2 hints {shape}")
