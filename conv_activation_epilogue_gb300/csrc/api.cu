@@ -109,6 +109,8 @@ CUtensorMapDataType tmap_type(mmact_dtype d)
 // not the memory), so encoded maps are kept in a small per-thread cache keyed
 // by every argument: a repeated call with the same tensors, shapes and dtypes
 // copies 128 bytes instead of encoding again, and a stale entry cannot exist.
+// A set-associative cache: the few maps of one call could share a slot of a
+// direct-mapped one and evict each other on every call.
 struct TmapKey {
     int32_t dt, rank, swizzle, pad;
     const void *ptr;
@@ -120,8 +122,11 @@ struct TmapEntry {
     TmapKey key;
     bool valid;
 };
-constexpr int TMAP_CACHE_ENTRIES = 256;      // direct-mapped, per host thread
-thread_local TmapEntry t_tmap_cache[TMAP_CACHE_ENTRIES];
+// 64 sets of 4 entries, per host thread: one call encodes at most 4 maps, so the
+// maps of a call never evict one another, whatever their hashes.
+constexpr int TMAP_SETS = 64, TMAP_WAYS = 4;
+thread_local TmapEntry t_tmap_cache[TMAP_SETS][TMAP_WAYS];
+thread_local uint8_t t_tmap_next[TMAP_SETS];   // way to replace next in each set (round robin)
 std::atomic<uint64_t> g_tmap_hits{0}, g_tmap_encodes{0};
 
 uint64_t tmap_hash(const TmapKey &k)
@@ -149,11 +154,14 @@ bool encode(CUtensorMap *m, mmact_dtype dt, int rank, const void *ptr, const uin
         k.es[i] = estrides ? estrides[i] : 1;
     }
     for (int i = 0; i + 1 < rank; ++i) k.gs[i] = strides_bytes[i];
-    TmapEntry &e = t_tmap_cache[tmap_hash(k) % TMAP_CACHE_ENTRIES];
-    if (e.valid && std::memcmp(&e.key, &k, sizeof(k)) == 0) {
-        *m = e.map;
-        g_tmap_hits.fetch_add(1, std::memory_order_relaxed);
-        return true;
+    const int set = (int)(tmap_hash(k) % TMAP_SETS);
+    for (int w = 0; w < TMAP_WAYS; ++w) {
+        const TmapEntry &e = t_tmap_cache[set][w];
+        if (e.valid && std::memcmp(&e.key, &k, sizeof(k)) == 0) {
+            *m = e.map;
+            g_tmap_hits.fetch_add(1, std::memory_order_relaxed);
+            return true;
+        }
     }
     CUresult r = g_encode(m, (CUtensorMapDataType)k.dt, (cuuint32_t)rank, const_cast<void *>(ptr), k.gd, k.gs,
                           k.bx, k.es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -161,6 +169,8 @@ bool encode(CUtensorMap *m, mmact_dtype dt, int rank, const void *ptr, const uin
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     g_tmap_encodes.fetch_add(1, std::memory_order_relaxed);
+    TmapEntry &e = t_tmap_cache[set][t_tmap_next[set]];
+    t_tmap_next[set] = (uint8_t)((t_tmap_next[set] + 1) % TMAP_WAYS);
     e.key = k;
     e.map = *m;
     e.valid = true;

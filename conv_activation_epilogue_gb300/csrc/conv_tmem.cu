@@ -388,7 +388,9 @@ __global__ void __launch_bounds__(TmemConvCfg<BN>::THREADS)
                 ptx::tc_fence_after();
                 const uint32_t d = pp.tmem + acc * BN;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!pipe_wait_spin(pp, afull0 + 8 * as, aph) || !pipe_wait(pp, pp.full0 + 8 * stage, phase)) {
+                    // the filter tile (normally landed long before) first, so that its wait
+                    // overlaps the previous block's MMAs; then the im2col tile
+                    if (!pipe_wait(pp, pp.full0 + 8 * stage, phase) || !pipe_wait_spin(pp, afull0 + 8 * as, aph)) {
                         ok = false;
                         break;
                     }
@@ -435,8 +437,8 @@ __global__ void __launch_bounds__(TmemConvCfg<BN>::THREADS)
                 const uint32_t stage = (uint32_t)(Gk % ASTAGES), phase = (uint32_t)((Gk / ASTAGES) & 1);
                 const uint32_t ws = (uint32_t)(Gk % WST), wph = (uint32_t)((Gk / WST) & 1);
                 const uint32_t tb = base + Cfg::OFF_TAB + 4u * (uint32_t)((kb % p.tab_period) * 64);
-                if (!warp_pipe_wait_spin(pp, wfull0 + 8 * ws, wph) ||
-                    !warp_pipe_wait_spin(pp, aempty0 + 8 * stage, phase ^ 1u)) {
+                if (!warp_pipe_wait_spin(pp, aempty0 + 8 * stage, phase ^ 1u) ||
+                    !warp_pipe_wait_spin(pp, wfull0 + 8 * ws, wph)) {
                     ok = false;
                     break;
                 }

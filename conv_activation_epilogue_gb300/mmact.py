@@ -241,19 +241,41 @@ def mmact_gemm_split_noalloc(A, B, bias, C, act: str = "none", alpha: float = 0.
            "mmact_gemm_split_noalloc")
 
 
+# ctypes int32 arrays for strides / pads / dilations, kept per value tuple: a call
+# site that repeats its geometry reuses them (the library only reads them during
+# the call)
+_I32_ARRAYS: dict = {}
+
+
 def _i32(vals, n):
     vals = tuple(int(v) for v in vals)
     if len(vals) != n:
         raise ValueError(f"expected {n} values")
-    return (ctypes.c_int32 * n)(*vals)
+    arr = _I32_ARRAYS.get(vals)
+    if arr is None:
+        if len(_I32_ARRAYS) > 1024:
+            _I32_ARRAYS.clear()
+        arr = _I32_ARRAYS[vals] = (ctypes.c_int32 * n)(*vals)
+    return arr
+
+
+_OUT_SHAPES: dict = {}
 
 
 def mmact_conv2d_out_shape(H, W, kh, kw, stride, pads, dilation) -> tuple:
+    """(Ho, Wo) from the library's output-size rule (answers kept per geometry)."""
+    key = (int(H), int(W), int(kh), int(kw), tuple(stride), tuple(pads), tuple(dilation))
+    hit = _OUT_SHAPES.get(key)
+    if hit is not None:
+        return hit
     L = load()
     ho, wo = ctypes.c_int64(), ctypes.c_int64()
     _check(L.mmact_conv2d_out_shape(H, W, kh, kw, _i32(stride, 2), _i32(pads, 4),
                                     _i32(dilation, 2), ctypes.byref(ho), ctypes.byref(wo)),
            "mmact_conv2d_out_shape")
+    if len(_OUT_SHAPES) > 1024:
+        _OUT_SHAPES.clear()
+    _OUT_SHAPES[key] = (ho.value, wo.value)
     return ho.value, wo.value
 
 

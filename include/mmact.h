@@ -448,8 +448,8 @@ mmact_status mmact_set_gemm_l2_policy(int mode);
 /*
  * Tensor-map cache counters (diagnostic; no counterpart in the pages).  Every
  * call encodes up to four TMA tensor maps on the host; an encoded map depends
- * only on its address, shape, strides, box and dtype, so the library keeps the
- * last 256 per host thread, keyed by all of them, and a call that repeats an
+ * only on its address, shape, strides, box and dtype, so the library keeps up
+ * to 256 per host thread (64 sets of 4), keyed by all of them, and a call that repeats an
  * earlier call's tensors and shapes copies them instead of encoding again.
  * Writes the process-wide number of cache hits and of encodes so far (either
  * pointer may be null).  Never fails.
