@@ -281,6 +281,7 @@ __global__ void __launch_bounds__(192, 1)
                     ptx::bulk_commit();
                 }
             }
+            if (!ok) break;                                 // a residual wait gave up
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
