@@ -65,7 +65,7 @@ extern "C" {
 typedef enum {
     MMACT_OK = 0,
     MMACT_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad enum, bad geometry */
-    MMACT_ERR_UNSUPPORTED = 2,   /* valid request this build does not handle (alignment, dtype pair) */
+    MMACT_ERR_UNSUPPORTED = 2,   /* valid request the library does not handle (alignment, dtype pair) */
     MMACT_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
     MMACT_ERR_TIMEOUT = 4        /* a kernel's bounded wait ran out (reported by get_last_error) */
 } mmact_status;
