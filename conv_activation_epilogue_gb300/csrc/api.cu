@@ -839,9 +839,10 @@ mmact_status nhwc_enqueue(const void *x, const void *w, const float *bias, void 
 // fused-versus-split grid on GB300 (GEMMs with K from 64 to 1024 and M, N
 // from 64 to 8192, small-channel convs; every activation) rather than from
 // an on-chip buffer budget.  The fused kernel wins on every shape with ReLU,
-// LeakyReLU, tanh and sigmoid (1.2x to 3.4x) and on every GEMM with GELU
-// whose output has more than 64 Ki elements (1.07x to 1.57x).  The split path
-// wins (a) with GELU on a small output (M*N <= 64 Ki: one or two tiles, where
+// LeakyReLU and tanh (1.2x to 3x) and on every GEMM with GELU whose output has
+// more than 512 Ki elements (1.04x to 1.36x); between 64 Ki and 512 Ki
+// elements the two are mixed (0.96x to 1.13x) and the fused kernel is kept.
+// The split path wins (a) with GELU on a small output (M*N <= 64 Ki: one or two tiles, where
 // the fused epilogue's few warps are latency-bound on the activation and the
 // split's activation pass spreads over the whole GPU; 64x64x64: 4.8 against
 // 5.7 us) and on small-channel convs with GELU (C*kh*kw <= 288, Co >= 64:

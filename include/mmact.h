@@ -153,7 +153,8 @@ mmact_status mmact_gemm_split(const void *A, const void *B, const float *bias, v
  * the split path is taken for GELU on an output of at most 65536 elements
  * (one or two tiles: the fused epilogue's few warps are latency-bound on the
  * activation, the split's activation pass spreads over the GPU), the fused
- * kernel everywhere else (1.07x to 3.4x faster there).  `workspace`
+ * kernel everywhere else (faster by up to 3x there, or within a few per cent
+ * on mid-sized GELU outputs).  `workspace`
  * ([M, N] fp32, 16-byte aligned) may be NULL: then the fused kernel always
  * runs.  Everything else as mmact_gemm / mmact_gemm_split.
  */
