@@ -94,3 +94,33 @@ def test_roofline_bound_follows_the_ridge_point():
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == PEAKS["hbm_gbs"]
     assert r["achieved"] == pytest.approx(b / 0.0300e-3 / 1e9)
     assert r["alg_bytes_per_launch"] == b
+
+
+def test_traffic_records_follow_their_kernels_sources(tmp_path, monkeypatch):
+    """A stored DRAM figure is reported only while every source its kernel depends on is
+    unchanged: each kernel hashes its own file plus the shared headers and the host planner."""
+    hashes = {k: bench.kernel_source_hash(k) for k in bench.KERNEL_FILES}
+    assert len(set(hashes.values())) == len(hashes)            # one hash per kernel
+    assert bench.kernel_source_hash("no_such_kernel") == bench.kernel_source_hash(None)
+    # every record committed in profiles/traffic.json matches the current sources
+    import json
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    for key, ent in rec.items():
+        kernel, workload = key.split("/")
+        assert kernel in bench.KERNEL_FILES and workload in synth.WORKLOADS
+        assert ent["dram_bytes_per_launch"] == ent["dram_read_bytes"] + ent["dram_write_bytes"]
+        assert bench.traffic_per_launch(kernel, workload) == ent["dram_bytes_per_launch"]
+    # a changed source voids the record: point the hash at a copy of the sources with one edit
+    src = os.path.join(bench.ROOT, "conv_activation_epilogue_gb300", "csrc")
+    fake = tmp_path / "conv_activation_epilogue_gb300" / "csrc"
+    fake.mkdir(parents=True)
+    for name in os.listdir(src):
+        if name.endswith((".cu", ".cuh", ".h")):
+            data = open(os.path.join(src, name), "rb").read()
+            if name == "gemm_pair.cu":
+                data += b"\n// edited\n"
+            (fake / name).write_bytes(data)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_source_hash("gemm_pair_kernel") != hashes["gemm_pair_kernel"]
+    assert bench.kernel_source_hash("conv_tmem_kernel") == hashes["conv_tmem_kernel"]
